@@ -1,0 +1,219 @@
+"""Python binding of libmoe.so: the single-GPU MoE stage1 + combine path.
+
+Argument marshalling only.  Every step of the path runs in the library's CUDA
+kernels; PyTorch supplies device memory and the current stream.  The functions
+carry the C entry points' names (include/moe.h) and take torch tensors.  There
+is no fallback: if the library is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import inputs  # noqa: F401  (seeded generators; no method arithmetic)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_EXPERT_ID, MOE_ERR_TIMEOUT = range(6)
+MOE_BLOCK_M = 128
+MOE_FLAGS_PER_TILE, MOE_FLAGS_PER_EXPERT = 0, 1
+MOE_SCHED_EXPERT_MAJOR, MOE_SCHED_READY_FIRST = 0, 1
+
+EXPORTS = [
+    "moe_status_string", "moe_layout_sizes", "moe_route_layout", "moe_dispatch_quant",
+    "moe_grouped_gemm1", "moe_combine", "moe_stage1", "moe_router_topk", "moe_quant_weights",
+    "moe_dequant_rows", "moe_device_sm_count",
+]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+
+
+class LayoutSizes(ctypes.Structure):
+    _fields_ = [("pairs", ctypes.c_int64), ("max_tiles", ctypes.c_int64), ("rowmap_len", ctypes.c_int64),
+                ("layout_ws_bytes", ctypes.c_size_t), ("stage1_ws_bytes", ctypes.c_size_t)]
+
+
+_TABLES = ["count", "expert_offset", "expert_tile_offset", "group_offset", "ready_tokens", "pair_row",
+           "row_pair", "row_weight", "rowmap", "tile_expert", "tile_row_begin", "tile_rows", "num_tiles",
+           "token_order"]
+
+
+class LayoutC(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "k", "E", "G", "block_m", "max_tiles")] + \
+               [(n, ctypes.c_void_p) for n in _TABLES]
+
+
+class Stage1Opts(ctypes.Structure):
+    _fields_ = [("comm_sms", ctypes.c_int32), ("flags", ctypes.c_int32), ("schedule", ctypes.c_int32),
+                ("producers_join", ctypes.c_int32), ("timeout_ns", ctypes.c_int64),
+                ("withhold_tile", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run __graft_entry__.build() first")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_status_string.argtypes = [i32]
+        L.moe_layout_sizes.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(LayoutSizes)]
+        L.moe_route_layout.argtypes = [vp, vp, ctypes.POINTER(LayoutC), vp, sz, vp, vp]
+        L.moe_dispatch_quant.argtypes = [vp, i32, ctypes.POINTER(LayoutC), vp, vp, vp, vp]
+        L.moe_grouped_gemm1.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(LayoutC), vp, vp, vp]
+        L.moe_combine.argtypes = [vp, i32, ctypes.POINTER(LayoutC), vp, vp, vp]
+        L.moe_stage1.argtypes = [vp, i32, ctypes.POINTER(LayoutC), vp, vp, i32, ctypes.POINTER(Stage1Opts),
+                                 vp, vp, vp, vp, sz, vp, vp]
+        L.moe_router_topk.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        L.moe_quant_weights.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        L.moe_dequant_rows.argtypes = [vp, vp, i32, ctypes.POINTER(LayoutC), vp, vp]
+        L.moe_device_sm_count.argtypes = []
+        for n in EXPORTS:
+            if n != "moe_status_string":
+                getattr(L, n).restype = i32
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().moe_status_string(int(code)).decode()
+
+
+def _check(fn: str, rc: int):
+    if rc != MOE_OK:
+        raise MoEError(fn, rc)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def moe_layout_sizes(T: int, k: int, E: int, G: int, block_m: int = MOE_BLOCK_M) -> LayoutSizes:
+    out = LayoutSizes()
+    _check("moe_layout_sizes", lib().moe_layout_sizes(T, k, E, G, block_m, ctypes.byref(out)))
+    return out
+
+
+class Layout:
+    """Device tables of one routing layout (torch-allocated) and their C struct."""
+
+    def __init__(self, T: int, k: int, E: int, G: int, device="cuda", block_m: int = MOE_BLOCK_M):
+        s = moe_layout_sizes(T, k, E, G, block_m)
+        self.T, self.k, self.E, self.G, self.block_m = T, k, E, G, block_m
+        self.max_tiles = int(s.max_tiles)
+        self.sizes = s
+        i32 = dict(dtype=torch.int32, device=device)
+        R = T * k
+        self.t = {
+            "count": torch.empty(E, **i32), "expert_offset": torch.empty(E + 1, **i32),
+            "expert_tile_offset": torch.empty(E + 1, **i32), "group_offset": torch.empty(G + 1, **i32),
+            "ready_tokens": torch.empty(E, **i32), "pair_row": torch.empty(R, **i32),
+            "row_pair": torch.empty(R, **i32), "row_weight": torch.empty(R, dtype=torch.float32, device=device),
+            "rowmap": torch.empty(self.max_tiles * block_m, **i32), "tile_expert": torch.empty(self.max_tiles, **i32),
+            "tile_row_begin": torch.empty(self.max_tiles, **i32), "tile_rows": torch.empty(self.max_tiles, **i32),
+            "num_tiles": torch.empty(1, **i32), "token_order": torch.empty(T, **i32),
+        }
+        self.ws = torch.empty(int(s.layout_ws_bytes), dtype=torch.uint8, device=device)
+        self.c = LayoutC(T, k, E, G, block_m, self.max_tiles, *[self.t[n].data_ptr() for n in _TABLES])
+
+    def __getitem__(self, name):
+        return self.t[name]
+
+    def numpy(self) -> dict:
+        return {n: v.cpu().numpy() for n, v in self.t.items()}
+
+
+def moe_route_layout(topk_ids: torch.Tensor, topk_w: torch.Tensor, layout: Layout, status: torch.Tensor,
+                     stream=None):
+    _check("moe_route_layout", lib().moe_route_layout(
+        _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(topk_w, torch.float32, "topk_w"), ctypes.byref(layout.c),
+        _ptr(layout.ws), layout.ws.numel(), _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def moe_dispatch_quant(x: torch.Tensor, layout: Layout, A: torch.Tensor, A_scale: torch.Tensor,
+                       status: torch.Tensor, stream=None):
+    _check("moe_dispatch_quant", lib().moe_dispatch_quant(
+        _ptr(x, torch.bfloat16, "x"), x.shape[1], ctypes.byref(layout.c), _ptr(A, torch.uint8, "A"),
+        _ptr(A_scale, torch.float32, "A_scale"), _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def moe_grouped_gemm1(A: torch.Tensor, A_scale: torch.Tensor, W: torch.Tensor, W_scale: torch.Tensor,
+                      layout: Layout, Y: torch.Tensor, status: torch.Tensor, stream=None):
+    E, N, H = W.shape
+    _check("moe_grouped_gemm1", lib().moe_grouped_gemm1(
+        _ptr(A, torch.uint8, "A"), _ptr(A_scale, torch.float32, "A_scale"), _ptr(W, torch.uint8, "W"),
+        _ptr(W_scale, torch.float32, "W_scale"), N, H, ctypes.byref(layout.c), _ptr(Y, torch.bfloat16, "Y"),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def moe_combine(Y: torch.Tensor, layout: Layout, out: torch.Tensor, status: torch.Tensor, stream=None):
+    _check("moe_combine", lib().moe_combine(
+        _ptr(Y, torch.bfloat16, "Y"), Y.shape[1], ctypes.byref(layout.c), _ptr(out, torch.bfloat16, "out"),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def stage1_opts(comm_sms=0, flags=MOE_FLAGS_PER_TILE, schedule=MOE_SCHED_EXPERT_MAJOR, producers_join=1,
+                timeout_ns=0, withhold_tile=-1) -> Stage1Opts:
+    return Stage1Opts(comm_sms, flags, schedule, producers_join, timeout_ns, withhold_tile, 0)
+
+
+def moe_stage1(x: torch.Tensor, layout: Layout, W: torch.Tensor, W_scale: torch.Tensor, A: torch.Tensor,
+               A_scale: torch.Tensor, Y: torch.Tensor, ws: torch.Tensor, status: torch.Tensor,
+               opts: Optional[Stage1Opts] = None, stream=None):
+    E, N, H = W.shape
+    opts = stage1_opts() if opts is None else opts
+    _check("moe_stage1", lib().moe_stage1(
+        _ptr(x, torch.bfloat16, "x"), H, ctypes.byref(layout.c), _ptr(W, torch.uint8, "W"),
+        _ptr(W_scale, torch.float32, "W_scale"), N, ctypes.byref(opts), _ptr(A, torch.uint8, "A"),
+        _ptr(A_scale, torch.float32, "A_scale"), _ptr(Y, torch.bfloat16, "Y"), _ptr(ws, torch.uint8, "ws"),
+        ws.numel(), _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def moe_router_topk(logits: torch.Tensor, k: int, topk_ids: torch.Tensor, topk_w: torch.Tensor, stream=None):
+    T, E = logits.shape
+    _check("moe_router_topk", lib().moe_router_topk(
+        _ptr(logits, torch.float32, "logits"), T, E, k, _ptr(topk_ids, torch.int32, "topk_ids"),
+        _ptr(topk_w, torch.float32, "topk_w"), _stream(stream)))
+
+
+def moe_quant_weights(W: torch.Tensor, Wq: torch.Tensor, W_scale: torch.Tensor, stream=None):
+    E, N, H = W.shape
+    _check("moe_quant_weights", lib().moe_quant_weights(
+        _ptr(W, torch.bfloat16, "W"), E, N, H, _ptr(Wq, torch.uint8, "Wq"),
+        _ptr(W_scale, torch.float32, "W_scale"), _stream(stream)))
+
+
+def moe_dequant_rows(A: torch.Tensor, A_scale: torch.Tensor, layout: Layout, Y: torch.Tensor, stream=None):
+    _check("moe_dequant_rows", lib().moe_dequant_rows(
+        _ptr(A, torch.uint8, "A"), _ptr(A_scale, torch.float32, "A_scale"), A.shape[1], ctypes.byref(layout.c),
+        _ptr(Y, torch.bfloat16, "Y"), _stream(stream)))
+
+
+def moe_device_sm_count() -> int:
+    return int(lib().moe_device_sm_count())

@@ -1,0 +1,298 @@
+// gemm1.cuh: the GEMM1 consumer pipeline (TMA producer thread, tcgen05 MMA
+// thread, promotion/epilogue warps) shared by moe_grouped_gemm1 and the fused
+// moe_stage1 kernel.
+//
+// GEMM1 of the mori stage1 page ("What": GEMM1 reads its A rows in place
+// through a rowmap; "How it works now": tiles in a static order gated per tile,
+// or in readiness order).  Work unit = (M-tile m, N-block nb): 128 dense rows
+// of one expert times 256 output columns, the full K = H.
+//
+// Per CTA (one per SM, 320 threads):
+//   warp 0, lane 0   claims units, publishes them through a shared-memory ring,
+//                    and streams the K-blocks (128 FP8 values of K) of A
+//                    (2-D TMA, rows [row0, row0+128) of the dense buffer, the
+//                    rowmap's first slot of the tile) and of W (3-D TMA, rows
+//                    [nb*256, +256) of expert e) into a 4-stage ring, 128-byte
+//                    swizzled.
+//   warp 1, lane 0   issues 4 tcgen05.mma (K=32 each, M=128, N=256, e4m3 x e4m3
+//                    -> fp32) per K-block into one of two TMEM partial buffers
+//                    (2 x 256 columns), committing to the smem-stage barrier
+//                    and the partial-ready barrier.
+//   warps 2..9       promotion: each thread owns one row (TMEM lane) and 128
+//                    columns; per K-block it loads the fp32 partial and folds it
+//                    into register accumulators with the two block scales,
+//                    acc += partial * (sa[row, kb] * sb[e, n/128, kb]); after the
+//                    last K-block it rounds to bf16 and stores the valid rows.
+//
+// fp32 block scales per 128 values are not a tensor-core mode (the hardware
+// block-scaled kinds take power-of-two scales per 32), so the scales are
+// applied in software on the CUDA cores, one FMA per accumulator per K-block,
+// overlapped with the next K-block's MMAs through the two TMEM buffers.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 256;
+constexpr int kGemmBK = 128;
+constexpr int kGemmStages = 4;
+constexpr int kGemmThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kUnitRing = 4;
+constexpr uint32_t kATileBytes = kGemmBM * kGemmBK;   // 16 KiB
+constexpr uint32_t kBTileBytes = kGemmBN * kGemmBK;   // 32 KiB
+constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
+constexpr uint32_t kTmemCols = 512;                   // two fp32 partial buffers of 256 columns
+constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kGemmBM, kGemmBN);
+
+struct GemmShared {
+  uint64_t full[kGemmStages];
+  uint64_t empty[kGemmStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t ufull[kUnitRing];
+  uint64_t uempty[kUnitRing];
+  uint64_t drain;
+  int4 unit[kUnitRing];     // {m (-1: end), nb, expert, row0}
+  int unit_rows[kUnitRing];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr size_t kGemmSmemBytes = 1024 + (size_t)kGemmStages * kStageBytes + sizeof(GemmShared);
+
+struct GemmParams {
+  const float* A_scale;   // [H/128][R]
+  const float* W_scale;   // [E][N/128][H/128]
+  LayoutDev L;
+  int N, H;
+  long long R;            // T*k: rows of A / Y
+  uint16_t* Y;            // [R][N]
+  int32_t* status;
+  uint64_t timeout_ns;
+};
+
+// Shared-memory carve-up: 1024-aligned stage buffers, then the barriers.
+struct GemmSmem {
+  uint8_t* stages;
+  GemmShared* sh;
+};
+
+MOE_DEV GemmSmem gemm_smem(uint8_t* raw) {
+  const uint32_t s = smem_u32(raw);
+  const uint32_t pad = (1024u - (s & 1023u)) & 1023u;
+  GemmSmem g;
+  g.stages = raw + pad;
+  g.sh = reinterpret_cast<GemmShared*>(g.stages + (size_t)kGemmStages * kStageBytes);
+  return g;
+}
+
+// Barrier init + TMEM allocation (whole CTA calls this).
+MOE_DEV void gemm_setup(const GemmSmem& S) {
+  GemmShared* sh = S.sh;
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGemmStages; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+    }
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(smem_u32(&sh->tfull[p]), 1);
+      mbar_init(smem_u32(&sh->tempty[p]), kEpiWarps);
+    }
+    for (int i = 0; i < kUnitRing; ++i) {
+      mbar_init(smem_u32(&sh->ufull[i]), 1);
+      mbar_init(smem_u32(&sh->uempty[i]), 1 + kEpiWarps);
+    }
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sh->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+MOE_DEV void gemm_teardown(const GemmSmem& S) {
+  tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(S.sh->tmem_base, kTmemCols);
+  }
+}
+
+// A unit handed from the producer thread to the MMA thread and the epilogue warps.
+struct Unit {
+  int m, nb, e, row0, rows;
+};
+
+// Producer side: publish unit j (m < 0 = end of work) into the ring.
+MOE_DEV bool publish_unit(GemmShared* sh, int j, const Unit& u, int32_t* status, uint64_t tmo) {
+  const int slot = j % kUnitRing;
+  const uint32_t ph = (uint32_t)(j / kUnitRing) & 1u;
+  if (!mbar_wait(smem_u32(&sh->uempty[slot]), ph ^ 1u, &sh->abort_flag, status, tmo)) return false;
+  sh->unit[slot] = make_int4(u.m, u.nb, u.e, u.row0);
+  sh->unit_rows[slot] = u.rows;
+  mbar_arrive(smem_u32(&sh->ufull[slot]));
+  return true;
+}
+
+// Stream the K-blocks of one unit into the stage ring.  `it` counts stage fills.
+MOE_DEV bool produce_unit(const GemmSmem& S, const CUtensorMap* tmA, const CUtensorMap* tmW,
+                          const Unit& u, int KB, uint32_t& it, int32_t* status, uint64_t tmo) {
+  GemmShared* sh = S.sh;
+  for (int kb = 0; kb < KB; ++kb) {
+    const int s = (int)(it % kGemmStages);
+    const uint32_t ph = (it / kGemmStages) & 1u;
+    if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, &sh->abort_flag, status, tmo)) return false;
+    const uint32_t full = smem_u32(&sh->full[s]);
+    mbar_arrive_expect_tx(full, kStageBytes);
+    const uint32_t dstA = smem_u32(S.stages + (size_t)s * kStageBytes);
+    tma_load_2d(dstA, tmA, kb * kGemmBK, u.row0, full);
+    tma_load_3d(dstA + kATileBytes, tmW, kb * kGemmBK, u.nb * kGemmBN, u.e, full);
+    ++it;
+  }
+  return true;
+}
+
+// Before leaving, wait (bounded, ignoring the abort flag) for the last fills in flight.
+MOE_DEV void drain_fills(const GemmSmem& S, uint32_t it, uint64_t tmo) {
+  int dummy_abort = 0;
+  const uint32_t first = it > (uint32_t)kGemmStages ? it - kGemmStages : 0u;
+  for (uint32_t i = first; i < it; ++i)
+    mbar_wait(smem_u32(&S.sh->full[i % kGemmStages]), (i / kGemmStages) & 1u, &dummy_abort, nullptr, tmo);
+}
+
+// MMA thread: consume units until the end marker.
+MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) {
+  GemmShared* sh = S.sh;
+  const uint32_t tmem = sh->tmem_base;
+  uint32_t it = 0, pit = 0;
+  bool issued = false;
+  for (int j = 0;; ++j) {
+    const int slot = j % kUnitRing;
+    if (!mbar_wait(smem_u32(&sh->ufull[slot]), (uint32_t)(j / kUnitRing) & 1u, &sh->abort_flag, status, tmo))
+      break;
+    const int m = sh->unit[slot].x;
+    mbar_arrive(smem_u32(&sh->uempty[slot]));
+    if (m < 0) break;
+    bool ok = true;
+    for (int kb = 0; kb < KB && ok; ++kb) {
+      const uint32_t p = pit & 1u, pph = (pit >> 1) & 1u;
+      const int s = (int)(it % kGemmStages);
+      const uint32_t ph = (it / kGemmStages) & 1u;
+      ok = mbar_wait(smem_u32(&sh->tempty[p]), pph ^ 1u, &sh->abort_flag, status, tmo) &&
+           mbar_wait(smem_u32(&sh->full[s]), ph, &sh->abort_flag, status, tmo);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(S.stages + (size_t)s * kStageBytes);
+      const uint32_t b0 = a0 + kATileBytes;
+#pragma unroll
+      for (int k4 = 0; k4 < kGemmBK / 32; ++k4)
+        umma_f8f6f4(tmem + p * kGemmBN, sw128_kmajor_desc(a0 + k4 * 32), sw128_kmajor_desc(b0 + k4 * 32),
+                    kIdesc, k4 > 0 ? 1u : 0u);
+      umma_commit(smem_u32(&sh->empty[s]));
+      umma_commit(smem_u32(&sh->tfull[p]));
+      issued = true;
+      ++it;
+      ++pit;
+    }
+    if (!ok) break;
+  }
+  if (issued) {   // no MMA may be in flight when TMEM is freed
+    int dummy_abort = 0;
+    umma_commit(smem_u32(&sh->drain));
+    mbar_wait(smem_u32(&sh->drain), 0u, &dummy_abort, nullptr, tmo);
+  }
+}
+
+// Promotion + epilogue warps (warps 2..9).  Returns when the end marker arrives.
+// `on_unit(m, e, rows)` lets the fused kernel acquire the tile's ready flag
+// before its first read of A_scale (always true for the unfused GEMM).
+template <typename OnUnit>
+MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_unit) {
+  GemmShared* sh = S.sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;                 // TMEM lane quarter this warp may access
+  const int h = (warp - 2) >> 2;          // column half: [h*128, h*128+128)
+  const int r_in_tile = q * 32 + lane;
+  const int KB = g.H / kGemmBK;
+  const int nsb = g.N / 128;
+  const uint32_t tmem = sh->tmem_base;
+  uint32_t pit = 0;
+  for (int j = 0;; ++j) {
+    const int slot = j % kUnitRing;
+    if (!mbar_wait(smem_u32(&sh->ufull[slot]), (uint32_t)(j / kUnitRing) & 1u, &sh->abort_flag, g.status,
+                   g.timeout_ns))
+      return;
+    const int4 un = sh->unit[slot];
+    const int rows = sh->unit_rows[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sh->uempty[slot]));
+    if (un.x < 0) return;
+    if (!on_unit(un.x, un.z, rows)) return;
+    const int nb = un.y, e = un.z, row0 = un.w;
+    const bool valid = r_in_tile < rows;
+    const float* sa_ptr = g.A_scale + row0 + r_in_tile;
+    const float* sb_ptr = g.W_scale + ((size_t)e * nsb + (size_t)nb * 2 + h) * KB;
+    float acc[128];
+#pragma unroll
+    for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+    float sa_n = valid ? __ldcg(sa_ptr) : 0.0f;
+    float sb_n = __ldg(sb_ptr);
+    for (int kb = 0; kb < KB; ++kb) {
+      const float sc = sa_n * sb_n;
+      if (kb + 1 < KB) {
+        sa_n = valid ? __ldcg(sa_ptr + (size_t)(kb + 1) * g.R) : 0.0f;
+        sb_n = __ldg(sb_ptr + kb + 1);
+      }
+      const uint32_t p = pit & 1u, pph = (pit >> 1) & 1u;
+      if (!mbar_wait(smem_u32(&sh->tfull[p]), pph, &sh->abort_flag, g.status, g.timeout_ns)) return;
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + p * kGemmBN + h * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32_wait(taddr + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], sc, acc[c * 32 + i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[p]));
+      ++pit;
+    }
+    if (valid) {
+      uint4* dst = reinterpret_cast<uint4*>(g.Y + (size_t)(row0 + r_in_tile) * g.N + (size_t)nb * kGemmBN + h * 128);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[8 * c + 0], acc[8 * c + 1]);
+        o.y = pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]);
+        o.z = pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]);
+        o.w = pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]);
+        dst[c] = o;
+      }
+    }
+  }
+}
+
+MOE_DEV Unit unit_of(const LayoutDev& L, int u, int nbn) {
+  Unit x;
+  x.m = u / nbn;
+  x.nb = u % nbn;
+  x.e = L.tile_expert[x.m];
+  x.row0 = L.rowmap[(size_t)x.m * kGemmBM];   // the tile's rows are contiguous from its first slot
+  x.rows = L.tile_rows[x.m];
+  return x;
+}
+
+}  // namespace moe

@@ -1,0 +1,429 @@
+// layout.cu: routing layout (stable counting sort of the T*k (token, slot)
+// pairs by (group, expert)) and the top-k router helper.
+//
+// The counting sort of the mori stage1 page ("How it works now": a counting
+// sort by (destination, first expert) so that a landed prefix of a run is a
+// prefix of experts; recv_layout commit: per-expert counts, padding of every
+// expert to the sort block, expert-major tables) as ONE cooperative launch:
+//
+//   phase A  each block histograms its contiguous token range: experts of its
+//            pairs and first (smallest) experts of its tokens, with
+//            warp-aggregated shared-memory adds (__match_any_sync leaders);
+//            the block's ids and weights stay staged in shared memory.
+//   barrier  one grid-wide barrier (bounded spin).
+//   phase B  every block scans the per-block histograms down its own column
+//            (its exclusive prefix per expert) and across experts (expert
+//            offsets, tile offsets, first-expert offsets) in shared memory;
+//            block 0 writes the E-sized tables, all blocks write tile tables
+//            and the rowmap grid-stride.
+//   phase C  stable ranks: warp 0 walks the block's pairs in (token, slot)
+//            order 32 at a time; lanes with equal experts find each other with
+//            __match_any_sync and take consecutive rows; warp 1 does the same
+//            for the token order by first expert.
+//
+// Logical group g holds experts [g*E/G, (g+1)*E/G) (the Mojo EPDispatchKernel
+// page's n_local_experts = n_experts / n_ranks), so the key (group, expert)
+// orders like the expert id.
+#include "common.cuh"
+#include "host_util.h"
+
+namespace moe {
+
+constexpr int kLayoutThreads = 512;
+constexpr int kLayoutMaxBlocks = 256;     // bound of the workspace's per-block histograms
+constexpr int kChunkPairs = 4096;         // pairs staged in shared memory per pass
+
+struct LayoutArgs {
+  const int32_t* ids;
+  const float* w;
+  LayoutDev L;
+  int32_t* ws_hist;     // [nblk][E]
+  int32_t* ws_fhist;    // [nblk][E]
+  uint32_t* ws_barrier; // zeroed in-stream before the launch
+  int32_t* status;
+  int tpb;              // tokens per block
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ int first_expert(const int32_t* s_ids, int k, int E) {
+  int fe = E;
+  for (int j = 0; j < k; ++j) {
+    int e = s_ids[j];
+    if (e >= 0 && e < E && e < fe) fe = e;
+  }
+  return fe;
+}
+
+// Exclusive scan over n <= 2*blockDim values held in shared memory (in place),
+// returning the total.  `scratch` holds >= 32 ints.
+__device__ int block_exclusive_scan(int* data, int n, int* scratch) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = blockDim.x >> 5;
+  int a = (2 * tid < n) ? data[2 * tid] : 0;
+  int b = (2 * tid + 1 < n) ? data[2 * tid + 1] : 0;
+  int v = a + b;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int s = lane < nw ? scratch[lane] : 0;
+    int si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int u = __shfl_up_sync(0xffffffffu, si, o);
+      if (lane >= o) si += u;
+    }
+    if (lane < nw) scratch[lane] = si - s;   // exclusive warp offsets
+    if (lane == 31) scratch[32] = si;        // total
+  }
+  __syncthreads();
+  int excl = scratch[warp] + incl - v;
+  if (2 * tid < n) data[2 * tid] = excl;
+  if (2 * tid + 1 < n) data[2 * tid + 1] = excl + a;
+  int total = scratch[32];
+  __syncthreads();
+  return total;
+}
+
+__global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs a) {
+  extern __shared__ int smem_i[];
+  const int E = a.L.E, k = a.L.k, T = a.L.T, BM = a.L.block_m;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x, nblk = gridDim.x;
+
+  int* hist = smem_i;             // [E]   block histogram, later the running row cursor
+  int* fhist = hist + E;          // [E]   block first-expert histogram, later the token cursor
+  int* eoff = fhist + E;          // [E+1] expert offsets
+  int* toff = eoff + E + 1;       // [E+1] expert tile offsets
+  int* foff = toff + E + 1;       // [E+1] first-expert offsets
+  int* scratch = foff + E + 1;    // [64]
+  int* s_ids = scratch + 64;      // [kChunkPairs]
+  float* s_w = reinterpret_cast<float*>(s_ids + kChunkPairs);  // [kChunkPairs]
+
+  const int t0 = min(T, b * a.tpb), t1 = min(T, t0 + a.tpb);
+  const int chunk_tokens = max(1, kChunkPairs / k);
+  const bool one_chunk = (t1 - t0) <= chunk_tokens;
+
+  for (int e = tid; e < E; e += blockDim.x) { hist[e] = 0; fhist[e] = 0; }
+  __syncthreads();
+
+  // ---------------- phase A: block histograms
+  for (int c0 = t0; c0 < t1; c0 += chunk_tokens) {
+    const int c1 = min(t1, c0 + chunk_tokens);
+    const int q0 = c0 * k, q1 = c1 * k;
+    for (int p = q0 + tid; p < q1; p += blockDim.x) {
+      s_ids[p - q0] = a.ids[p];
+      s_w[p - q0] = a.w[p];
+    }
+    __syncthreads();
+    for (int base = q0; base < q1; base += blockDim.x) {
+      const int p = base + tid;
+      int e = -1;
+      if (p < q1) {
+        e = s_ids[p - q0];
+        if (e < 0 || e >= E) { set_status(a.status, MOE_ERR_EXPERT_ID); e = -1; }
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[e], __popc(peers));
+    }
+    for (int base = c0; base < c1; base += blockDim.x) {
+      const int t = base + tid;
+      int fe = -1;
+      if (t < c1) {
+        fe = first_expert(s_ids + (t - c0) * k, k, E);
+        if (fe >= E) fe = -1;
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, fe);
+      if (fe >= 0 && lane == __ffs(peers) - 1) atomicAdd(&fhist[fe], __popc(peers));
+    }
+    __syncthreads();
+  }
+  for (int e = tid; e < E; e += blockDim.x) {
+    a.ws_hist[(size_t)b * E + e] = hist[e];
+    a.ws_fhist[(size_t)b * E + e] = fhist[e];
+  }
+
+  // ---------------- grid-wide barrier (all blocks are co-resident: cooperative launch)
+  __syncthreads();
+  if (tid == 0) {
+    int timed_out = 0;
+    __threadfence();
+    atomicAdd(a.ws_barrier, 1u);
+    const uint64_t tstart = globaltimer_ns();
+    while (true) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.ws_barrier) : "memory");
+      if (v >= (unsigned)nblk) break;
+      if (globaltimer_ns() - tstart > a.timeout_ns) {
+        set_status(a.status, MOE_ERR_TIMEOUT);
+        timed_out = 1;
+        break;
+      }
+      __nanosleep(64);
+    }
+    scratch[63] = timed_out;
+  }
+  __syncthreads();
+  if (scratch[63] == 1) return;
+
+  // ---------------- phase B: column prefixes and expert scans
+  for (int e = tid; e < E; e += blockDim.x) {
+    int pre = 0, tot = 0, fpre = 0, ftot = 0;
+    for (int bb = 0; bb < nblk; ++bb) {
+      const int h = __ldcg(a.ws_hist + (size_t)bb * E + e);
+      const int f = __ldcg(a.ws_fhist + (size_t)bb * E + e);
+      if (bb < b) { pre += h; fpre += f; }
+      tot += h;
+      ftot += f;
+    }
+    hist[e] = pre;      // this block's first row within expert e (relative)
+    fhist[e] = fpre;    // this block's first position within first-expert e (relative)
+    eoff[e] = tot;
+    toff[e] = (tot + BM - 1) / BM;
+    foff[e] = ftot;
+  }
+  __syncthreads();
+  const int total_rows = block_exclusive_scan(eoff, E, scratch);
+  const int total_tiles = block_exclusive_scan(toff, E, scratch);
+  const int total_first = block_exclusive_scan(foff, E, scratch);
+  if (tid == 0) { eoff[E] = total_rows; toff[E] = total_tiles; foff[E] = total_first; }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    hist[e] += eoff[e];
+    fhist[e] += foff[e];
+  }
+  if (b == 0) {
+    for (int e = tid; e <= E; e += blockDim.x) {
+      if (e < E) {
+        a.L.count[e] = eoff[e + 1] - eoff[e];
+        a.L.ready_tokens[e] = foff[e + 1];
+      }
+      a.L.expert_offset[e] = eoff[e];
+      a.L.expert_tile_offset[e] = toff[e];
+    }
+    const int epg = E / a.L.G;
+    for (int g = tid; g <= a.L.G; g += blockDim.x) a.L.group_offset[g] = eoff[g * epg];
+    if (tid == 0) a.L.num_tiles[0] = total_tiles;
+  }
+  // tile tables and rowmap, grid-stride over all blocks
+  {
+    const int gtid = b * blockDim.x + tid, gstride = nblk * blockDim.x;
+    const int cap = a.L.max_tiles;
+    for (int m = gtid; m < cap; m += gstride) {
+      int e = -1, begin = T * k, rows = 0;
+      if (m < total_tiles) {
+        int lo = 0, hi = E;                 // largest e with toff[e] <= m
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (toff[mid] <= m) lo = mid; else hi = mid;
+        }
+        e = lo;
+        const int i = m - toff[e];
+        begin = eoff[e] + i * BM;
+        rows = min(BM, eoff[e + 1] - begin);
+      }
+      a.L.tile_expert[m] = e;
+      a.L.tile_row_begin[m] = begin;
+      a.L.tile_rows[m] = rows;
+    }
+    const long long slots = (long long)cap * BM;
+    for (long long s = gtid; s < slots; s += gstride) {
+      const int m = (int)(s / BM), j = (int)(s % BM);
+      int v = -1;
+      if (m < total_tiles) {
+        int lo = 0, hi = E;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (toff[mid] <= m) lo = mid; else hi = mid;
+        }
+        const int begin = eoff[lo] + (m - toff[lo]) * BM;
+        if (begin + j < eoff[lo + 1]) v = begin + j;
+      }
+      a.L.rowmap[s] = v;
+    }
+  }
+  __syncthreads();
+
+  // ---------------- phase C: stable ranks within the block
+  for (int c0 = t0; c0 < t1; c0 += chunk_tokens) {
+    const int c1 = min(t1, c0 + chunk_tokens);
+    const int q0 = c0 * k, q1 = c1 * k;
+    if (!one_chunk) {
+      __syncthreads();
+      for (int p = q0 + tid; p < q1; p += blockDim.x) {
+        s_ids[p - q0] = a.ids[p];
+        s_w[p - q0] = a.w[p];
+      }
+      __syncthreads();
+    }
+    if (warp == 0) {
+      for (int base = q0; base < q1; base += 32) {
+        const int p = base + lane;
+        int e = -1;
+        if (p < q1) {
+          e = s_ids[p - q0];
+          if (e < 0 || e >= E) { a.L.pair_row[p] = -1; e = -1; }
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0) {
+          const int row = hist[e] + __popc(peers & lanemask_lt());
+          a.L.pair_row[p] = row;
+          a.L.row_pair[row] = p;
+          a.L.row_weight[row] = s_w[p - q0];
+        }
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) hist[e] += __popc(peers);
+        __syncwarp();
+      }
+    } else if (warp == 1) {
+      for (int base = c0; base < c1; base += 32) {
+        const int t = base + lane;
+        int fe = -1;
+        if (t < c1) {
+          fe = first_expert(s_ids + (t - c0) * k, k, E);
+          if (fe >= E) fe = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, fe);
+        if (fe >= 0) a.L.token_order[fhist[fe] + __popc(peers & lanemask_lt())] = t;
+        __syncwarp();
+        if (fe >= 0 && lane == __ffs(peers) - 1) fhist[fe] += __popc(peers);
+        __syncwarp();
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- router helper
+
+// One warp per token: k rounds of a warp-wide arg-max (largest logit, ties to
+// the lower expert id), then softmax weights over the selected logits.
+template <int VPL>
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T,
+                                                          int E, int k, int32_t* __restrict__ ids,
+                                                          float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps) {
+    float v[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = i * 32 + lane;
+      v[i] = e < E ? logits[(size_t)t * E + e] : -INFINITY;
+    }
+    bool used[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) used[i] = (i * 32 + lane) >= E;
+    float sel_l0 = 0.f, my_l = 0.f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+      float best = -INFINITY;
+      int bid = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = i * 32 + lane;
+        if (!used[i] && (v[i] > best || (v[i] == best && e < bid))) { best = v[i]; bid = e; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bid, o);
+        if (ob > best || (ob == best && oi < bid)) { best = ob; bid = oi; }
+      }
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        if (i * 32 + lane == bid) used[i] = true;
+      if (j == 0) sel_l0 = best;
+      if (lane == j) { my_l = best; my_id = bid; }
+    }
+    const float ex = lane < k ? expf(my_l - sel_l0) : 0.f;
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);   // slots in order
+    if (lane < k) {
+      ids[(size_t)t * k + lane] = my_id;
+      w[(size_t)t * k + lane] = ex / sum;
+    }
+  }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+static size_t layout_smem_bytes(int E) {
+  return sizeof(int) * (size_t)(2 * E + 3 * (E + 1) + 64 + kChunkPairs) + sizeof(float) * kChunkPairs;
+}
+
+size_t moe_layout_ws_bytes(int E) {
+  return 256 + 2 * sizeof(int32_t) * (size_t)kLayoutMaxBlocks * E;
+}
+
+extern "C" int moe_route_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
+                                void* ws, size_t ws_bytes, int32_t* status, moe_stream_t stream) {
+  int rc = check_layout(L);
+  if (rc) return rc;
+  if (!topk_ids || !topk_w || !ws) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_layout_ws_bytes(L->E)) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)ws & 15) != 0) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int dev, nsm;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+
+  const size_t smem = layout_smem_bytes(L->E);
+  static_assert(kLayoutThreads * 2 >= 1024, "scan covers E <= 1024");
+  if (cudaFuncSetAttribute(route_layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_layout_kernel, kLayoutThreads, smem) != cudaSuccess || per_sm < 1)
+    return MOE_ERR_CUDA;
+  // one block per SM at most, at least ~32 tokens per block
+  int nblk = (L->T + 31) / 32;
+  nblk = std::min(nblk, std::min(nsm * per_sm, std::min(nsm, kLayoutMaxBlocks)));
+  nblk = std::max(nblk, 1);
+  const int tpb = (L->T + nblk - 1) / nblk;
+  nblk = (L->T + tpb - 1) / tpb;
+
+  LayoutArgs a;
+  a.ids = topk_ids;
+  a.w = topk_w;
+  a.L = to_dev(L);
+  a.ws_barrier = reinterpret_cast<uint32_t*>(ws);
+  a.ws_hist = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + 256);
+  a.ws_fhist = a.ws_hist + (size_t)kLayoutMaxBlocks * L->E;
+  a.status = status;
+  a.tpb = tpb;
+  a.timeout_ns = 1000000000ull;
+
+  if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nblk);
+  cfg.blockDim = dim3(kLayoutThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, route_layout_kernel, a) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+extern "C" int moe_router_topk(const float* logits, int T, int E, int k, int32_t* topk_ids,
+                               float* topk_w, moe_stream_t stream) {
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int warps = 8;
+  const int grid = std::min((T + warps - 1) / warps, 4096);
+  if (E <= 256)
+    router_topk_kernel<8><<<grid, warps * 32, 0, s>>>(logits, T, E, k, topk_ids, topk_w);
+  else
+    router_topk_kernel<32><<<grid, warps * 32, 0, s>>>(logits, T, E, k, topk_ids, topk_w);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -1,0 +1,221 @@
+/*
+ * moe.h: C ABI of the single-GPU MoE stage1 + combine library (libmoe.so, sm_103a).
+ *
+ * The path: a stable counting-sort routing layout of each token's top-k
+ * (expert, weight) pairs; a dispatch that quantises each token once to FP8
+ * e4m3 with fp32 per-128 block scales and scatters it into its expert-major
+ * rows; GEMM1 as a grouped FP8 GEMM that reads those rows in place; a fused
+ * stage1 that overlaps the dispatch (producer SMs) with GEMM1 (consumer SMs)
+ * through per-tile ready flags; and a combine that gathers each token's k
+ * expert outputs back into token order, weighted by the router weights.
+ *
+ * Sources, by page title and section:
+ *  [mori]     "poc(cco): MegaMoE stage1 dispatch over SDMA" (mori PR #1).
+ *  [mojo]     "EPDispatchKernel" (Mojo ep_comm API page).
+ *  [tilepipe] "TilePipe: MoE Communication and Overlap Kernels with CuteDSL".
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers are device memory owned by the caller;
+ *    the library never allocates, frees or keeps them, and keeps no global
+ *    mutable state.  Host pointers (struct arguments) are read during the call
+ *    only.
+ *  - bf16 tensors are passed as uint16_t bit patterns; fp8 tensors as uint8_t
+ *    e4m3 codes ("fn" variant: no infinities, max 448).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; 0 = legacy default
+ *    stream) and never synchronises the host.  Calls capture into CUDA graphs.
+ *  - The return code reports argument and launch errors found on the host.
+ *    Errors found on the device are written to `*status` (a device int32 that
+ *    the caller zeroes; the first error wins) and are read after a sync.
+ *  - One call at a time per workspace: two calls that share a workspace or
+ *    output buffers must be ordered on one stream.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t;   /* same handle as cudaStream_t */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, workspace too small */
+  MOE_ERR_UNSUPPORTED = 2,   /* device is not sm_100-class / shape beyond a kernel limit */
+  MOE_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  MOE_ERR_EXPERT_ID = 4,     /* device: an expert id outside [0, E); the pair was skipped */
+  MOE_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up (stage1 flag never set) */
+} moe_status;
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(int status);
+
+/* Sort block: rows per GEMM1 M-tile and padding unit of every expert
+ * ([mori] recv_layout commit: each expert padded to the sort block of 128). */
+#define MOE_BLOCK_M 128
+/* Quantisation block along the hidden dimension (fp32 scale per 128 values). */
+#define MOE_QBLOCK 128
+
+/* ---------------------------------------------------------------------------
+ * Sizes.  One function sizes every table and workspace; the kernels index them
+ * with the same numbers.
+ *   T tokens, k routes per token, E experts in G logical groups (group g holds
+ *   experts [g*E/G, (g+1)*E/G): [mojo] n_local_experts = n_experts / n_ranks).
+ * Limits: 1 <= T <= 2^20, 1 <= k <= 32, k <= E <= 1024, E % G == 0,
+ * T*k < 2^31, block_m == 128.
+ * ------------------------------------------------------------------------- */
+typedef struct moe_layout_sizes {
+  int64_t pairs;             /* T*k: rows of the dense dispatch buffer */
+  int64_t max_tiles;         /* min(T*k, (T*k + E*(block_m-1)) / block_m) */
+  int64_t rowmap_len;        /* max_tiles * block_m */
+  size_t layout_ws_bytes;    /* workspace for moe_route_layout */
+  size_t stage1_ws_bytes;    /* workspace for moe_stage1 */
+} moe_layout_sizes_t;
+
+int moe_layout_sizes(int T, int k, int E, int G, int block_m, moe_layout_sizes_t* out);
+
+/* ---------------------------------------------------------------------------
+ * Layout tables ([mori] recv_layout commit: counts per expert, padding to the
+ * sort block, rowmap / srcmap / weights / tile tables; [mojo] ep_final_layout:
+ * each routed row written to its final contiguous per-expert row).
+ * The caller fills the shape fields and the device pointers (sizes from
+ * moe_layout_sizes); moe_route_layout writes the tables, the other calls read
+ * them.  Pair p = t*k + j is token t's j-th route.
+ * ------------------------------------------------------------------------- */
+typedef struct moe_layout {
+  int32_t T, k, E, G, block_m, max_tiles;          /* host values */
+  int32_t* count;              /* [E]   pairs routed to expert e */
+  int32_t* expert_offset;      /* [E+1] exclusive prefix of count: first dense row of e */
+  int32_t* expert_tile_offset; /* [E+1] exclusive prefix of ceil(count/block_m) */
+  int32_t* group_offset;       /* [G+1] expert_offset[g*E/G]: a group's run of rows */
+  int32_t* ready_tokens;       /* [E]   inclusive prefix of first-expert counts */
+  int32_t* pair_row;           /* [T*k] dense row of pair p (-1 if its id was invalid) */
+  int32_t* row_pair;           /* [T*k] pair held by dense row r */
+  float* row_weight;           /* [T*k] router weight of the pair held by row r */
+  int32_t* rowmap;             /* [max_tiles*block_m] dense row of tile slot, or -1 */
+  int32_t* tile_expert;        /* [max_tiles] expert of tile m, -1 past num_tiles */
+  int32_t* tile_row_begin;     /* [max_tiles] first dense row of tile m, T*k past num_tiles */
+  int32_t* tile_rows;          /* [max_tiles] valid rows of tile m (1..block_m), 0 past num_tiles */
+  int32_t* num_tiles;          /* [1]   tiles in use */
+  int32_t* token_order;        /* [T]   tokens stably sorted by first (smallest) expert */
+} moe_layout_t;
+
+/* moe_route_layout: histogram, prefix sums and stable ranks of the T*k pairs
+ * sorted by (group, expert), rows within an expert in ascending pair order
+ * ([mori] "How it works now": counting sort so that a landed prefix of a run
+ * is a prefix of experts).  Also the token order by first expert that the
+ * stage1 producer walks, so that every token of expert e sits before
+ * ready_tokens[e].
+ *   topk_ids  device int32 [T, k] row-major; ids outside [0,E) are skipped and
+ *             raise MOE_ERR_EXPERT_ID in *status (the tables then cover only
+ *             the valid pairs).
+ *   topk_w    device f32 [T, k] router weights (copied to row_weight).
+ *   ws        device workspace of at least layout_ws_bytes (contents ignored;
+ *             the call initialises what it uses, in-stream).
+ * One launch (a cooperative grid with one grid-wide barrier). */
+int moe_route_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
+                     void* ws, size_t ws_bytes, int32_t* status, moe_stream_t stream);
+
+/* moe_dispatch_quant: quantise each token once and store it to each of its k
+ * rows ([mori] "How it works now" and the quant-once commit: read and quantise
+ * a token once, store it to every run it is in).  Per token t and block b of
+ * 128 values: amax = max|x|, scale = amax/448 (fp32), code = e4m3(x/scale)
+ * (fp32 IEEE division, round to nearest even, saturating); amax == 0 gives
+ * scale 0 and zero codes.
+ *   x        device bf16 [T, H] row-major, H % 128 == 0, H <= 32768.
+ *   A        device u8 [T*k, H] row-major: row pair_row[t*k+j] = codes of token t.
+ *   A_scale  device f32 [H/128, T*k]: A_scale[b*T*k + r] = scale of row r, block b.
+ * Rows of invalid pairs are not written. */
+int moe_dispatch_quant(const uint16_t* x, int H, const moe_layout_t* L, uint8_t* A,
+                       float* A_scale, int32_t* status, moe_stream_t stream);
+
+/* moe_grouped_gemm1: Y[r, n] = bf16( sum_k (A[r,k]*sa[r,k/128]) * (W[e,n,k]*sb[e,n/128,k/128]) )
+ * for every dense row r of expert e ([mori] "What": GEMM1 reads its A rows in
+ * place through the rowmap).  One persistent tcgen05 kernel: M-tiles of 128
+ * rows from the tile tables in expert-major order, FP8 operands by TMA,
+ * fp32 accumulation with the block scales applied per 128 of K.
+ *   A, A_scale  as written by moe_dispatch_quant (A must be 16-byte aligned).
+ *   W           device u8 [E, N, H] e4m3 codes, row n of expert e is K-contiguous.
+ *   W_scale     device f32 [E, N/128, H/128].
+ *   Y           device bf16 [T*k, N] row-major; only valid rows are written.
+ * N % 256 == 0, H % 128 == 0, N, H <= 32768. */
+int moe_grouped_gemm1(const uint8_t* A, const float* A_scale, const uint8_t* W,
+                      const float* W_scale, int N, int H, const moe_layout_t* L, uint16_t* Y,
+                      int32_t* status, moe_stream_t stream);
+
+/* moe_combine: out[t, :] = bf16( sum_{j<k} w[t,j] * Y[pair_row[t*k+j], :] ),
+ * accumulated in fp32 with the slots in ascending order; w is read as
+ * row_weight[pair_row[t*k+j]] ([tilepipe] "Communication Kernels": the
+ * combine that returns expert outputs to token order).
+ *   Y    device bf16 [T*k, D] (D % 8 == 0), out device bf16 [T, D].
+ * A pair whose pair_row is -1 contributes nothing. */
+int moe_combine(const uint16_t* Y, int D, const moe_layout_t* L, uint16_t* out, int32_t* status,
+                moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Fused stage1 ([tilepipe] "Overlap": SMs partitioned between a producer that
+ * bumps a semaphore per finished tile and a consumer GEMM waiting on it,
+ * producer order chosen to unblock the expert-major GEMM order as early as
+ * possible, sync granularity per tile or per expert; [mori] "How it works
+ * now": GEMM1 gated per tile on ready signals, or --ready-first, a scheduler
+ * publishing m-tiles in readiness order with workers taking tickets).
+ * Computes exactly what moe_dispatch_quant followed by moe_grouped_gemm1 does
+ * (same A, A_scale and Y bits), in one cooperative launch of one CTA per SM.
+ * ------------------------------------------------------------------------- */
+typedef enum moe_flag_granularity { MOE_FLAGS_PER_TILE = 0, MOE_FLAGS_PER_EXPERT = 1 } moe_flag_granularity;
+typedef enum moe_schedule { MOE_SCHED_EXPERT_MAJOR = 0, MOE_SCHED_READY_FIRST = 1 } moe_schedule;
+
+typedef struct moe_stage1_opts {
+  int32_t comm_sms;          /* producer CTAs (1..#SMs-1); 0 = default (16) */
+  int32_t flags;             /* moe_flag_granularity */
+  int32_t schedule;          /* moe_schedule */
+  int32_t producers_join;    /* 1: producer CTAs take GEMM work once their tokens are done */
+  int64_t timeout_ns;        /* bound of every wait on a flag; 0 = default (1 s) */
+  int32_t withhold_tile;     /* test hook: >= 0 never publishes this M-tile's rows (the
+                                consumer must time out); -1 = off */
+  int32_t reserved;
+} moe_stage1_opts_t;
+
+/*   x, H, L        as moe_dispatch_quant; W, W_scale, N as moe_grouped_gemm1.
+ *   A, A_scale, Y  outputs as the unfused calls.
+ *   ws             device workspace of at least stage1_ws_bytes (initialised
+ *                  in-stream by the call). */
+int moe_stage1(const uint16_t* x, int H, const moe_layout_t* L, const uint8_t* W,
+               const float* W_scale, int N, const moe_stage1_opts_t* opts, uint8_t* A,
+               float* A_scale, uint16_t* Y, void* ws, size_t ws_bytes, int32_t* status,
+               moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Helpers (input preparation and the identity expert of the bandwidth sweep).
+ * ------------------------------------------------------------------------- */
+
+/* moe_router_topk: per token, the k largest of E logits (ties to the lower
+ * expert id; slots in descending order) and weights softmax-renormalised over
+ * the k selected: w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0) in fp32.
+ *   logits device f32 [T, E] (E <= 1024); topk_ids device int32 [T, k];
+ *   topk_w device f32 [T, k]. */
+int moe_router_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                    moe_stream_t stream);
+
+/* moe_quant_weights: expert weights bf16 [E, N, H] -> e4m3 codes [E, N, H]
+ * and fp32 scales [E, N/128, H/128], one scale per 128x128 block with the
+ * activations' amax/448 rule.  N % 128 == 0, H % 128 == 0. */
+int moe_quant_weights(const uint16_t* W, int E, int N, int H, uint8_t* Wq, float* W_scale,
+                      moe_stream_t stream);
+
+/* moe_dequant_rows: the identity expert, Y[r, :] = bf16(code * scale) for every
+ * valid dense row r (Y device bf16 [T*k, H]). */
+int moe_dequant_rows(const uint8_t* A, const float* A_scale, int H, const moe_layout_t* L,
+                     uint16_t* Y, moe_stream_t stream);
+
+/* Number of SMs of the current device (0 on error): the persistent grids'
+ * size. */
+int moe_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -1,0 +1,138 @@
+"""GPU parity of the FP8 dispatch (bit-exact codes and scales), the weight
+quantiser (bit-exact), the identity expert (bit-exact) and the combine
+(stated tolerance) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import combine_counting_sort_gb300 as moe
+import oracle
+from combine_counting_sort_gb300 import inputs
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    gu.build()
+
+
+def dispatch_on_gpu(cfg, x):
+    ids, w = gu.routed(cfg)
+    L, status = gu.gpu_layout(ids, w, cfg.E, cfg.G)
+    R = cfg.T * cfg.k
+    A = torch.full((R, cfg.H), 0x7F, dtype=torch.uint8, device="cuda")           # poison (NaN code)
+    As = torch.full((cfg.H // 128, R), float("nan"), dtype=torch.float32, device="cuda")
+    moe.moe_dispatch_quant(x.cuda(), L, A, As, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    return ids, w, L, A, As
+
+
+@pytest.mark.parametrize("name", ["tiny", "t2048_uniform", "t8192_zipf1.2"])
+def test_dispatch_matches_oracle_bit_exact(name):
+    cfg = inputs.CONFIGS[name]
+    x = inputs.make_x(cfg.T, cfg.H, cfg.seed)
+    ids, w, L, A, As = dispatch_on_gpu(cfg, x)
+    q, s = oracle.quantize_rows(inputs.bf16_bits(x))
+    A_ref, As_ref = oracle.dispatch(q, s, L["pair_row"].cpu().numpy(), cfg.k)
+    assert np.array_equal(A.cpu().numpy(), A_ref)
+    assert np.array_equal(As.cpu().numpy().view(np.uint32), As_ref.view(np.uint32))
+
+
+def test_dispatch_special_blocks_bit_exact():
+    # zero blocks, constant blocks, signed zeros, exact grid values, subnormal-range values, ragged T
+    T, H, E, G, k = 45, 640, 6, 3, 3
+    rng = np.random.default_rng(5)
+    xv = rng.standard_normal((T, H))
+    xv[0] = 0.0
+    xv[1, :128] = -0.0
+    xv[2, 128:256] = 3.0
+    xv[3] *= 1e-30
+    xv[4, :127] = oracle.e4m3_decode(np.arange(127, dtype=np.uint8)) * 2.0 ** -5
+    xv[5] *= 1e4
+    xb = oracle.f64_to_bf16(xv)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    w = np.full((T, k), 1.0 / k, np.float32)
+    L, status = gu.gpu_layout(ids, w, E, G)
+    R = T * k
+    A = torch.empty((R, H), dtype=torch.uint8, device="cuda")
+    As = torch.empty((H // 128, R), dtype=torch.float32, device="cuda")
+    moe.moe_dispatch_quant(x.cuda(), L, A, As, status)
+    torch.cuda.synchronize()
+    q, s = oracle.quantize_rows(xb)
+    A_ref, As_ref = oracle.dispatch(q, s, L["pair_row"].cpu().numpy(), k)
+    assert np.array_equal(A.cpu().numpy(), A_ref)
+    assert np.array_equal(As.cpu().numpy().view(np.uint32), As_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("E,N,H", [(2, 256, 384), (3, 512, 1024)])
+def test_weight_quant_bit_exact(E, N, H):
+    W = inputs.make_weights(E, N, H, seed=2)
+    Wq = torch.empty(E, N, H, dtype=torch.uint8, device="cuda")
+    Ws = torch.empty(E, N // 128, H // 128, dtype=torch.float32, device="cuda")
+    moe.moe_quant_weights(W.cuda(), Wq, Ws)
+    torch.cuda.synchronize()
+    q, s = oracle.quantize_weights(inputs.bf16_bits(W))
+    assert np.array_equal(Wq.cpu().numpy(), q)
+    assert np.array_equal(Ws.cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
+def test_identity_expert_bit_exact():
+    cfg = inputs.CONFIGS["tiny"]
+    x = inputs.make_x(cfg.T, cfg.H, cfg.seed)
+    ids, w, L, A, As = dispatch_on_gpu(cfg, x)
+    Y = torch.empty(cfg.T * cfg.k, cfg.H, dtype=torch.bfloat16, device="cuda")
+    moe.moe_dequant_rows(A, As, L, Y)
+    torch.cuda.synchronize()
+    R = cfg.T * cfg.k
+    assert np.array_equal(gu.bits(Y), oracle.identity_expert(A.cpu().numpy(), As.cpu().numpy(), np.arange(R)))
+
+
+@pytest.mark.parametrize("name", ["tiny", "bw_t2048"])
+def test_dispatch_identity_combine(name):
+    cfg = inputs.CONFIGS[name]
+    x = inputs.make_x(cfg.T, cfg.H, cfg.seed)
+    ids, w, L, A, As = dispatch_on_gpu(cfg, x)
+    R = cfg.T * cfg.k
+    Y = torch.empty(R, cfg.H, dtype=torch.bfloat16, device="cuda")
+    moe.moe_dequant_rows(A, As, L, Y)
+    out = torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_combine(Y, L, out, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    Y_ref = oracle.identity_expert(A.cpu().numpy(), As.cpu().numpy(), np.arange(R))
+    assert np.array_equal(gu.bits(Y), Y_ref)
+    ref = oracle.combine(Y_ref, L["pair_row"].cpu().numpy(), w)
+    gu.assert_close_bf16(gu.bits(out), ref, "combine")
+    # the invariant: weights summing to one bring back the dequantised input
+    q, s = oracle.quantize_rows(inputs.bf16_bits(x))
+    deq = (oracle.e4m3_decode(q).reshape(cfg.T, -1, 128) * s.astype(np.float64)[:, :, None]).reshape(cfg.T, -1)
+    gu.assert_close_bf16(gu.bits(out), oracle.f64_to_bf16(deq), "dispatch->identity->combine")
+
+
+@pytest.mark.parametrize("T,k,D", [(1, 1, 8), (33, 3, 200), (257, 8, 4096), (100, 12, 1032)])
+def test_combine_random_matches_oracle(T, k, D):
+    rng = np.random.default_rng(T * k)
+    E = max(k, 16)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    w = rng.random((T, k)).astype(np.float32)
+    w /= w.sum(1, keepdims=True)
+    L, status = gu.gpu_layout(ids, w, E, 1)
+    Yb = oracle.f64_to_bf16(rng.standard_normal((T * k, D)))
+    Y = torch.from_numpy(Yb.view(np.int16)).view(torch.bfloat16).cuda()
+    out = torch.empty(T, D, dtype=torch.bfloat16, device="cuda")
+    moe.moe_combine(Y, L, out, status)
+    torch.cuda.synchronize()
+    ref = oracle.combine(Yb, L["pair_row"].cpu().numpy(), w)
+    gu.assert_close_bf16(gu.bits(out), ref, "combine")
+    # one-hot weights: an exact gather
+    onehot = np.zeros_like(w)
+    onehot[np.arange(T), np.arange(T) % k] = 1.0
+    L2, _ = gu.gpu_layout(ids, onehot, E, 1)
+    moe.moe_combine(Y, L2, out, status)
+    torch.cuda.synchronize()
+    assert np.array_equal(gu.bits(out), oracle.combine(Yb, L2["pair_row"].cpu().numpy(), onehot))
