@@ -1,0 +1,466 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE stage1 + combine hot path on GB300.
+
+One step = the whole hot path over one batch of T tokens: routing layout
+(moe_route_layout) -> fused quant + dispatch + GEMM1 (moe_stage1) -> weighted
+combine (moe_combine), all in the library's kernels on one stream, inputs
+resident in HBM.  Default workload: T=8192 tokens, H=7168, 256 experts in 8
+groups, top-8, GEMM1 N=4096, Zipf(1.2) expert popularity (synthetic, seeded).
+
+Prints ONE JSON line (rank 0).  `value` is tokens/s of the step; per-kernel
+microseconds, GEMM1 TFLOP/s and dispatch/combine GB/s ride along.  `--impl
+reference` times the CPU oracle on a bounded sample of the same workload.
+
+Multi-GPU: replicas only (every rank runs the same single-GPU workload; the
+path has no data exchange), launched by torchrun; the max over ranks of the
+timed region gives the whole-job throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "stage1 µs & tokens/s at T=8192 (GEMM1 TFLOP/s); dispatch/combine HBM GB/s"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2
+FP8_OVER_BF16 = 2.0                 # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Max over ranks of a per-rank float (identity on one rank)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.p = None
+        self.gpu = gpu_index
+        if enabled:
+            try:
+                self.p = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                     "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < len(CLOCK_FIELDS):
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- the GPU arm
+
+class Workload:
+    """Device-resident inputs and buffers of one workload."""
+
+    def __init__(self, cfg, device, stage1_opts):
+        import combine_counting_sort_gb300 as moe
+        from combine_counting_sort_gb300 import inputs
+        self.moe, self.cfg, self.dev = moe, cfg, device
+        T, H, E, G, k, N = cfg.T, cfg.H, cfg.E, cfg.G, cfg.k, cfg.N
+        self.R = T * k
+        self.x = inputs.make_x(T, H, cfg.seed).to(device)
+        logits = inputs.make_logits(T, E, cfg.zipf, cfg.seed).to(device)
+        self.ids = torch.empty(T, k, dtype=torch.int32, device=device)
+        self.w = torch.empty(T, k, dtype=torch.float32, device=device)
+        moe.moe_router_topk(logits, k, self.ids, self.w)
+        W = inputs.make_weights(E, N, H, cfg.seed, device=device)
+        self.Wq = torch.empty(E, N, H, dtype=torch.uint8, device=device)
+        self.Ws = torch.empty(E, N // 128, H // 128, dtype=torch.float32, device=device)
+        moe.moe_quant_weights(W, self.Wq, self.Ws)
+        torch.cuda.synchronize(device)
+        del W
+        self.L = moe.Layout(T, k, E, G, device=device)
+        self.A = torch.empty(self.R, H, dtype=torch.uint8, device=device)
+        self.As = torch.empty(H // 128, self.R, dtype=torch.float32, device=device)
+        self.Y = torch.empty(self.R, N, dtype=torch.bfloat16, device=device)
+        self.out = torch.empty(T, N, dtype=torch.bfloat16, device=device)
+        self.ws = torch.empty(int(self.L.sizes.stage1_ws_bytes), dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.opts = stage1_opts
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        torch.cuda.empty_cache()
+
+    def step(self, s, ev=None, fused=True, ids=None, w=None):
+        """One pass of the hot path on stream s; ev = 4 events (layout | stage1 | combine)."""
+        moe = self.moe
+        ids = self.ids if ids is None else ids
+        w = self.w if w is None else w
+        if ev: ev[0].record(s)
+        moe.moe_route_layout(ids, w, self.L, self.status, stream=s)
+        if ev: ev[1].record(s)
+        if fused:
+            moe.moe_stage1(self.x, self.L, self.Wq, self.Ws, self.A, self.As, self.Y, self.ws, self.status,
+                           self.opts, stream=s)
+        else:
+            moe.moe_dispatch_quant(self.x, self.L, self.A, self.As, self.status, stream=s)
+            if ev and len(ev) > 4: ev[4].record(s)
+            moe.moe_grouped_gemm1(self.A, self.As, self.Wq, self.Ws, self.L, self.Y, self.status, stream=s)
+        if ev: ev[2].record(s)
+        moe.moe_combine(self.Y, self.L, self.out, self.status, stream=s)
+        if ev: ev[3].record(s)
+
+    def flush_l2(self, s):
+        with torch.cuda.stream(s):
+            self.flush.zero_()
+
+    # algorithmic work per launch
+    def gemm_flops(self):
+        return 2.0 * self.R * self.cfg.N * self.cfg.H
+
+    def dispatch_bytes(self):
+        c = self.cfg
+        return 2.0 * c.T * c.H + self.R * c.H + 4.0 * self.R * c.H / 128
+
+    def combine_bytes(self):
+        c = self.cfg
+        return 2.0 * self.R * c.N + 2.0 * c.T * c.N + 8.0 * self.R
+
+
+def timed_loop(wl, s, steps, fused, n_ev):
+    evs = []
+    for _ in range(steps):
+        wl.flush_l2(s)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+        wl.step(s, ev, fused=fused)
+        evs.append(ev)
+    torch.cuda.synchronize()
+    return evs
+
+
+def run_gpu(args):
+    import combine_counting_sort_gb300 as moe
+    from combine_counting_sort_gb300 import inputs
+    import __graft_entry__ as ge
+
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    ge.build()
+    cfg = inputs.CONFIGS[args.workload]
+    opts = moe.stage1_opts(comm_sms=args.comm_sms, flags=args.flags, schedule=args.schedule,
+                           producers_join=args.join)
+    wl = Workload(cfg, device, opts)
+    s = torch.cuda.Stream(device)
+    fused = args.variant == "fused"
+
+    for _ in range(args.warmup):
+        wl.flush_l2(s)
+        wl.step(s, fused=fused)
+    torch.cuda.synchronize()
+    if wl.status.item() != 0:
+        raise RuntimeError(f"device status {moe.status_string(wl.status.item())} after warm-up")
+
+    # ---- timed region: exactly K steps, barrier + sync on both sides
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    t_wall = time.perf_counter()
+    evs = timed_loop(wl, s, args.steps, fused, 4)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    clk = clocks.stop()
+    if wl.status.item() != 0:
+        raise RuntimeError(f"device status {moe.status_string(wl.status.item())} in the timed region")
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    layout_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    stage_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = reduce_max(sum(step_ms), world, device)
+    ms_per_step = total_ms / args.steps
+    value = world * cfg.T / (ms_per_step / 1e3)
+
+    # ---- the unfused chain of the same step, for the fused-vs-sum comparison
+    uev = timed_loop(wl, s, max(3, args.steps // 2), False, 5)
+    u_disp = statistics.median(e[1].elapsed_time(e[4]) for e in uev)
+    u_gemm = statistics.median(e[4].elapsed_time(e[2]) for e in uev)
+
+    # ---- end to end through the public API with host buffers: H2D inputs, D2H output
+    e2e = run_e2e(wl, s, args, world, device)
+
+    peaks = measured_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    stage_avg = statistics.mean(stage_ms) if fused else u_gemm
+    achieved = wl.gemm_flops() / (stage_avg / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate, bf16 out)",
+        "data": "synthetic (seeded: x~N(0,1) bf16, logits~N(0,1)+Zipf bias, W1~N(0,1/H) quantised on device)",
+        "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "G": cfg.G, "k": cfg.k, "N": cfg.N,
+                   "zipf": cfg.zipf, "step": "route_layout + stage1 (%s) + combine" % args.variant,
+                   "stage1_opts": {"comm_sms": args.comm_sms, "flags": ["per_tile", "per_expert"][args.flags],
+                                   "schedule": ["expert_major", "ready_first"][args.schedule],
+                                   "producers_join": args.join},
+                   "l2": "flushed between steps (512 MiB write, outside the step events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "stage1_kernel" if fused else "grouped_gemm1_kernel", "bound": "tensor",
+                     "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / fp8_peak, 4),
+                     "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (fp8/bf16 nominal)",
+                     "traffic": args.traffic},
+        "stage1_us": round(statistics.median(stage_ms) * 1e3, 1),
+        "layout_us": round(statistics.median(layout_ms) * 1e3, 1),
+        "combine_us": round(statistics.median(comb_ms) * 1e3, 1),
+        "unfused_us": {"dispatch": round(u_disp * 1e3, 1), "gemm1": round(u_gemm * 1e3, 1),
+                       "sum": round((u_disp + u_gemm) * 1e3, 1)},
+        "gemm1_tflops": round(wl.gemm_flops() / (u_gemm / 1e3) / 1e12, 1),
+        "stage1_tflops": round(wl.gemm_flops() / (statistics.median(stage_ms) / 1e3) / 1e12, 1),
+        "dispatch_gbs": round(wl.dispatch_bytes() / (u_disp / 1e3) / 1e9, 1),
+        "combine_gbs": round(wl.combine_bytes() / (statistics.median(comb_ms) / 1e3) / 1e9, 1),
+        "hbm_peak_gbs": peaks["hbm_gbs"],
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_budget_s)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(wl, s, args, world, device):
+    """Same step through the public API with pinned host buffers: H2D of x and the
+    router's pairs, the path, D2H of the combined output, all inside the events."""
+    T, H, k, N = wl.cfg.T, wl.cfg.H, wl.cfg.k, wl.cfg.N
+    hx = wl.x.cpu().pin_memory()
+    hids = wl.ids.cpu().pin_memory()
+    hw = wl.w.cpu().pin_memory()
+    hout = torch.empty(T, N, dtype=torch.bfloat16).pin_memory()
+    dx, dids, dw = torch.empty_like(wl.x), torch.empty_like(wl.ids), torch.empty_like(wl.w)
+    x_saved = wl.x
+    steps = max(3, args.steps // 2)
+    evs = []
+    wl.x = dx
+    try:
+        for i in range(steps + 2):
+            wl.flush_l2(s)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            with torch.cuda.stream(s):
+                dx.copy_(hx, non_blocking=True)
+                dids.copy_(hids, non_blocking=True)
+                dw.copy_(hw, non_blocking=True)
+            wl.step(s, fused=args.variant == "fused", ids=dids, w=dw)
+            with torch.cuda.stream(s):
+                hout.copy_(wl.out, non_blocking=True)
+            e1.record(s)
+            if i >= 2:
+                evs.append((e0, e1))
+        torch.cuda.synchronize()
+    finally:
+        wl.x = x_saved
+    ms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in evs), world, device)
+    bi = hx.numel() * 2 + hids.numel() * 4 + hw.numel() * 4
+    bo = hout.numel() * 2
+    return {"value": round(world * T / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 4)}
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+
+class CpuSample:
+    """The oracle, as it stands, on a bounded sample of the workload.
+
+    Untimed set-up: inputs, the router's top-k pairs (input preparation, not a
+    step of the path) and the sample experts' weights as random finite e4m3
+    codes with fp32 block scales (weights are quantised offline; the oracle's
+    time does not depend on their values).  Timed: the routing layout of all T
+    tokens, then quant + dispatch + GEMM1 + combine over the rows of the first
+    non-empty experts in expert-major order until the budget is spent."""
+
+    def __init__(self, cfg):
+        import numpy as np
+        import oracle
+        from combine_counting_sort_gb300 import inputs
+        self.np, self.oracle, self.cfg = np, oracle, cfg
+        self.x = inputs.bf16_bits(inputs.make_x(cfg.T, cfg.H, cfg.seed))
+        logits = inputs.make_logits(cfg.T, cfg.E, cfg.zipf, cfg.seed).numpy()
+        self.ids, self.w = oracle.router_topk(logits, cfg.k)
+        self.rng = np.random.default_rng(cfg.seed)
+        self.weights = {}
+
+    def expert_weights(self, e):
+        np, cfg = self.np, self.cfg
+        if e not in self.weights:
+            codes = self.rng.integers(0, 0x7E, size=(1, cfg.N, cfg.H), dtype=np.uint8)
+            codes |= (self.rng.integers(0, 2, size=codes.shape, dtype=np.uint8) << 7)
+            scales = np.full((1, cfg.N // 128, cfg.H // 128), 1.0 / (448.0 * math.sqrt(cfg.H)), np.float32)
+            self.weights[e] = (codes, scales)
+        return self.weights[e]
+
+    def run(self, budget_s: float):
+        np, oracle, cfg = self.np, self.oracle, self.cfg
+        timed = 0.0
+        t0 = time.perf_counter()
+        L = oracle.route_layout(self.ids, self.w, cfg.E, cfg.G)
+        timed += time.perf_counter() - t0
+        eo = L["expert_offset"]
+        rows_done, experts_done = 0, 0
+        for e in range(cfg.E):
+            if eo[e + 1] == eo[e]:
+                continue
+            Wq, Ws = self.expert_weights(e)
+            t0 = time.perf_counter()
+            rows = np.arange(eo[e], eo[e + 1])
+            pairs = L["row_pair"][rows]
+            toks, inv = np.unique(pairs // cfg.k, return_inverse=True)
+            q, sc = oracle.quantize_rows(self.x[toks])
+            A, As = q[inv], np.ascontiguousarray(sc[inv].T)         # dispatch of the sample rows
+            Yb = oracle.grouped_gemm1(A, As, Wq, Ws, np.array([0, len(rows)]))
+            # combine work of these rows: each row weighted into its token's accumulator
+            oracle.combine(Yb, np.arange(len(rows)), np.asarray(L["row_weight"][rows], np.float32)[:, None])
+            timed += time.perf_counter() - t0
+            rows_done += len(rows)
+            experts_done += 1
+            if timed > budget_s:
+                break
+        tok_per_s = (rows_done / cfg.k) / timed
+        desc = (f"timed: layout of all {cfg.T} tokens + quant/dispatch/GEMM1/combine over the rows of the first "
+                f"{experts_done} non-empty experts ({rows_done} of {cfg.T * cfg.k} rows); value = rows/k per second")
+        return tok_per_s, desc, timed
+
+
+def cpu_baseline(cfg, budget_s):
+    v, desc, el = CpuSample(cfg).run(budget_s)
+    return {"value": round(v, 2), "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": desc, "seconds": round(el, 2)}
+
+
+def run_reference(args):
+    """Reference arm of this tier: the CPU oracle timed on the host cores."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from combine_counting_sort_gb300 import inputs
+    cfg = inputs.CONFIGS[args.workload]
+    per_step = max(2.0, args.cpu_budget_s / max(1, args.steps))
+    sample = CpuSample(cfg)
+    sample.run(0.5)                      # warm-up: one expert
+    vals, descs, secs = [], [], 0.0
+    for _ in range(args.steps):
+        v, d, el = sample.run(per_step)
+        vals.append(v)
+        descs.append(d)
+        secs += el
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 quant)",
+            "data": "synthetic (seeded)", "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E,
+                                                      "G": cfg.G, "k": cfg.k, "N": cfg.N, "zipf": cfg.zipf},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+                             "kind": "oracle", "sample": descs[-1]},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="t8192_zipf1.2")
+    ap.add_argument("--variant", choices=["fused", "unfused"], default="fused")
+    ap.add_argument("--comm-sms", type=int, default=16)
+    ap.add_argument("--flags", type=int, default=0, help="0 per-tile, 1 per-expert")
+    ap.add_argument("--schedule", type=int, default=0, help="0 expert-major, 1 ready-first")
+    ap.add_argument("--join", type=int, default=1, help="producer CTAs take GEMM work when done")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch of the roofline kernel from an ncu capture (else null)")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

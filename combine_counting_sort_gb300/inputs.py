@@ -14,6 +14,8 @@ Workloads (hidden size H, experts E in G logical groups, top-k, GEMM1 width N):
 * ``bw_t{2048,4096,8192,16384}``: dispatch + combine bandwidth sweep with the
   identity expert (no GEMM), uniform routing.
 * ``stage1_t16384_zipf1.0``: fused stage1 workload, T=16384, Zipf(s=1.0).
+* ``profile_t8192_e32``: the T=8192 shapes with 32 experts, small enough for
+  multi-pass profiler captures.
 
 The shapes (hidden 7168, 256 routed experts, top-8, two 2048-wide projections)
 are those of the DeepSeek-V3-class models the mori stage1 page benchmarks
@@ -60,6 +62,8 @@ CONFIGS = {
     "bw_t16384": MoEConfig("bw_t16384", T=16384, H=7168, E=256, G=8, k=8, N=7168, gemm=False),
     "stage1_t16384_zipf1.0": MoEConfig("stage1_t16384_zipf1.0", T=16384, H=7168, E=256, G=8, k=8,
                                        N=4096, zipf=1.0),
+    # profiler-sized: the T=8192 shapes with 32 experts (weights 0.5 GB instead of 7.5 GB)
+    "profile_t8192_e32": MoEConfig("profile_t8192_e32", T=8192, H=7168, E=32, G=8, k=8, N=4096, zipf=1.2),
 }
 
 
