@@ -26,7 +26,7 @@ MOE_SCHED_EXPERT_MAJOR, MOE_SCHED_READY_FIRST = 0, 1
 EXPORTS = [
     "moe_status_string", "moe_layout_sizes", "moe_route_layout", "moe_dispatch_quant",
     "moe_grouped_gemm1", "moe_combine", "moe_stage1", "moe_router_topk", "moe_quant_weights",
-    "moe_dequant_rows", "moe_device_sm_count",
+    "moe_dequant_rows", "moe_device_sm_count", "moe_route_layout_noalloc",
 ]
 
 
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
         L.moe_quant_weights.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.moe_dequant_rows.argtypes = [vp, vp, i32, ctypes.POINTER(LayoutC), vp, vp]
         L.moe_device_sm_count.argtypes = []
+        L.moe_route_layout_noalloc.argtypes = [vp, vp, ctypes.POINTER(LayoutC), vp, vp]
         for n in EXPORTS:
             if n != "moe_status_string":
                 getattr(L, n).restype = i32
@@ -154,6 +155,16 @@ def moe_route_layout(topk_ids: torch.Tensor, topk_w: torch.Tensor, layout: Layou
     _check("moe_route_layout", lib().moe_route_layout(
         _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(topk_w, torch.float32, "topk_w"), ctypes.byref(layout.c),
         _ptr(layout.ws), layout.ws.numel(), _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def moe_route_layout_noalloc(topk_ids: torch.Tensor, topk_w: torch.Tensor, layout: Layout, status: torch.Tensor,
+                             stream=None):
+    """moe_route_layout without a workspace: for callers that cannot allocate
+    device memory, the scratch is a fixed array inside the library (E <= 256).
+    Calls that can overlap on the GPU share that array and must be ordered."""
+    _check("moe_route_layout_noalloc", lib().moe_route_layout_noalloc(
+        _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(topk_w, torch.float32, "topk_w"), ctypes.byref(layout.c),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
 
 
 def moe_dispatch_quant(x: torch.Tensor, layout: Layout, A: torch.Tensor, A_scale: torch.Tensor,

@@ -427,3 +427,98 @@ extern "C" int moe_router_topk(const float* logits, int T, int E, int k, int32_t
     router_topk_kernel<32><<<grid, warps * 32, 0, s>>>(logits, T, E, k, topk_ids, topk_w);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
+
+// ---------------------------------------------------------------- allocation-free variant
+//
+// moe_route_layout_noalloc: the same layout kernel, with its scratch in a
+// fixed device array of this library instead of a caller workspace, for
+// callers that cannot allocate device memory: a plugin inside a framework
+// whose memory pool owns the whole device, a latency-critical path that must
+// not pay the device-wide synchronisation a cudaMalloc can cause, or a
+// deployment that sizes all memory once at load time.  The array (512 KiB +
+// 256 B, for up to 256 experts) is reserved on every GPU that loads the
+// library and stays there until the process exits.  The first call on a
+// device looks its address up (make that call outside any stream capture);
+// every call shares the array, so calls that can overlap on the GPU race.
+
+namespace moe {
+constexpr int kNoAllocMaxExperts = MOE_NOALLOC_MAX_EXPERTS;
+// header (grid-barrier counter) + two per-block histograms of up to kLayoutMaxBlocks x 256 experts
+constexpr size_t kNoAllocScratchBytes = 256 + 2 * sizeof(int32_t) * (size_t)kLayoutMaxBlocks * kNoAllocMaxExperts;
+}  // namespace moe
+
+static __device__ __align__(256) unsigned char g_layout_scratch[moe::kNoAllocScratchBytes];
+
+#include <mutex>
+
+// Device address of g_layout_scratch on each device, looked up once per device
+// (the symbol's name is only a host-side handle; kernels need this address).
+static void* g_scratch_addr[128];
+static std::mutex g_scratch_mu;
+
+static int layout_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_layout_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return MOE_OK;
+}
+
+extern "C" int moe_route_layout_noalloc(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
+                                        int32_t* status, moe_stream_t stream) {
+  int rc = check_layout(L);
+  if (rc) return rc;
+  if (!topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (L->E > kNoAllocMaxExperts) return MOE_ERR_UNSUPPORTED;   // beyond the fixed scratch
+  void* ws = nullptr;
+  rc = layout_scratch_address(&ws);
+  if (rc) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  int dev, nsm;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+
+  const size_t smem = layout_smem_bytes(L->E);
+  if (cudaFuncSetAttribute(route_layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_layout_kernel, kLayoutThreads, smem) != cudaSuccess || per_sm < 1)
+    return MOE_ERR_CUDA;
+  int nblk = (L->T + 31) / 32;
+  nblk = std::min(nblk, std::min(nsm * per_sm, std::min(nsm, kLayoutMaxBlocks)));
+  nblk = std::max(nblk, 1);
+  const int tpb = (L->T + nblk - 1) / nblk;
+  nblk = (L->T + tpb - 1) / tpb;
+
+  LayoutArgs a;
+  a.ids = topk_ids;
+  a.w = topk_w;
+  a.L = to_dev(L);
+  a.ws_barrier = reinterpret_cast<uint32_t*>(ws);
+  a.ws_hist = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + 256);
+  a.ws_fhist = a.ws_hist + (size_t)kLayoutMaxBlocks * L->E;
+  a.status = status;
+  a.tpb = tpb;
+  a.timeout_ns = 1000000000ull;
+
+  // the array keeps the previous call's contents: the barrier counter must start at zero
+  // (the histograms are fully written before they are read)
+  if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nblk);
+  cfg.blockDim = dim3(kLayoutThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, route_layout_kernel, a) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}

@@ -17,8 +17,9 @@
  * Conventions for every entry point:
  *  - Pointers named as device pointers are device memory owned by the caller;
  *    the library never allocates, frees or keeps them, and keeps no global
- *    mutable state.  Host pointers (struct arguments) are read during the call
- *    only.
+ *    mutable state (the one exception is the fixed scratch array behind
+ *    moe_route_layout_noalloc).  Host pointers (struct arguments) are read
+ *    during the call only.
  *  - bf16 tensors are passed as uint16_t bit patterns; fp8 tensors as uint8_t
  *    e4m3 codes ("fn" variant: no infinities, max 448).
  *  - Every call is asynchronous on `stream` (a cudaStream_t; 0 = legacy default
@@ -118,6 +119,25 @@ typedef struct moe_layout {
  * One launch (a cooperative grid with one grid-wide barrier). */
 int moe_route_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
                      void* ws, size_t ws_bytes, int32_t* status, moe_stream_t stream);
+
+/* moe_route_layout_noalloc: moe_route_layout for callers that cannot
+ * allocate device memory: a plugin inside a framework whose memory pool owns
+ * the whole device (a raw cudaMalloc would fail or fragment the pool), a
+ * latency-critical path that must not pay the device-wide synchronisation a
+ * cudaMalloc can cause, or a deployment that sizes all memory once at load
+ * time.  The scratch lives in a fixed array inside this library, so the
+ * caller passes only inputs and outputs.  The source pages have no
+ * counterpart of this entry point.
+ *   Limit: E <= MOE_NOALLOC_MAX_EXPERTS (larger E returns MOE_ERR_UNSUPPORTED);
+ *   other limits and outputs as moe_route_layout.
+ *   The array (about 512 KiB) is reserved on every GPU that loads the library
+ *   until the process exits.  The first call on each device looks up the
+ *   array's device address; make that first call outside any stream capture.
+ *   All calls share the one array: calls that can overlap on the GPU (other
+ *   streams, other threads) race and must be ordered by the caller. */
+#define MOE_NOALLOC_MAX_EXPERTS 256
+int moe_route_layout_noalloc(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
+                             int32_t* status, moe_stream_t stream);
 
 /* moe_dispatch_quant: quantise each token once and store it to each of its k
  * rows ([mori] "How it works now" and the quant-once commit: read and quantise
