@@ -54,7 +54,7 @@ class LayoutC(ctypes.Structure):
 class Stage1Opts(ctypes.Structure):
     _fields_ = [("comm_sms", ctypes.c_int32), ("flags", ctypes.c_int32), ("schedule", ctypes.c_int32),
                 ("producers_join", ctypes.c_int32), ("timeout_ns", ctypes.c_int64),
-                ("withhold_tile", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("withhold_tile", ctypes.c_int32), ("trace", ctypes.c_int32)]
 
 
 _lib = None
@@ -190,8 +190,22 @@ def moe_combine(Y: torch.Tensor, layout: Layout, out: torch.Tensor, status: torc
 
 
 def stage1_opts(comm_sms=0, flags=MOE_FLAGS_PER_TILE, schedule=MOE_SCHED_EXPERT_MAJOR, producers_join=1,
-                timeout_ns=0, withhold_tile=-1) -> Stage1Opts:
-    return Stage1Opts(comm_sms, flags, schedule, producers_join, timeout_ns, withhold_tile, 0)
+                timeout_ns=0, withhold_tile=-1, trace=0) -> Stage1Opts:
+    return Stage1Opts(comm_sms, flags, schedule, producers_join, timeout_ns, withhold_tile, trace)
+
+
+TRACE_SLOTS = ["start", "produced", "wait_ns", "waited_units", "end", "joined_units", "units"]
+
+
+def stage1_trace(ws: torch.Tensor) -> dict:
+    """Trace slots of a stage1 workspace after a call with trace=1 (synchronises):
+    times in microseconds from the kernel start, counters as integers."""
+    v = ws[64:64 + 8 * len(TRACE_SLOTS)].view(torch.int64).cpu().tolist()
+    d = dict(zip(TRACE_SLOTS, v))
+    t0 = d["start"]
+    return {"produced_us": (d["produced"] - t0) / 1e3, "end_us": (d["end"] - t0) / 1e3,
+            "wait_us_total": d["wait_ns"] / 1e3, "waited_units": d["waited_units"],
+            "joined_units": d["joined_units"], "units": d["units"]}
 
 
 def moe_stage1(x: torch.Tensor, layout: Layout, W: torch.Tensor, W_scale: torch.Tensor, A: torch.Tensor,

@@ -27,8 +27,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int KB = g.H / kGemmBK;
   const int units = g.L.num_tiles[0] * nbn;
 
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp < kEpiWarp0) {
+    regs_dealloc<kRegsControl>();
+    if (warp == 0 && lane == 0) {
       uint32_t it = 0;
       int j = 0;
       bool ok = true;
@@ -42,10 +43,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         publish_unit(S.sh, j, end, g.status, g.timeout_ns);
       }
       drain_fills(S, it, g.timeout_ns);
+    } else if (warp == 1 && lane == 0) {
+      mma_loop(S, KB, g.status, g.timeout_ns);
     }
-  } else if (warp == 1) {
-    if (lane == 0) mma_loop(S, KB, g.status, g.timeout_ns);
   } else {
+    regs_alloc<kRegsEpilogue>();
     epilogue_loop(S, g, [](int, int, int) { return true; });
   }
   gemm_teardown(S);

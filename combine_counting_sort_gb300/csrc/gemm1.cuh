@@ -7,7 +7,7 @@
 // or in readiness order).  Work unit = (M-tile m, N-block nb): 128 dense rows
 // of one expert times 256 output columns, the full K = H.
 //
-// Per CTA (one per SM, 320 threads):
+// Per CTA (one per SM, 384 threads = 3 warpgroups):
 //   warp 0, lane 0   claims units, publishes them through a shared-memory ring,
 //                    and streams the K-blocks (128 FP8 values of K) of A
 //                    (2-D TMA, rows [row0, row0+128) of the dense buffer, the
@@ -18,7 +18,9 @@
 //                    -> fp32) per K-block into one of two TMEM partial buffers
 //                    (2 x 256 columns), committing to the smem-stage barrier
 //                    and the partial-ready barrier.
-//   warps 2..9       promotion: each thread owns one row (TMEM lane) and 128
+//   warps 2, 3       idle (they complete warpgroup 0, whose registers go to
+//                    the promotion warpgroups: setmaxnreg 40 / 232).
+//   warps 4..11      promotion: each thread owns one row (TMEM lane) and 128
 //                    columns; per K-block it loads the fp32 partial and folds it
 //                    into register accumulators with the two block scales,
 //                    acc += partial * (sa[row, kb] * sb[e, n/128, kb]); after the
@@ -31,6 +33,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "tmem_fold.cuh"
 
 namespace moe {
 
@@ -38,8 +41,16 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 256;
 constexpr int kGemmBK = 128;
 constexpr int kGemmStages = 4;
-constexpr int kGemmThreads = 320;
+constexpr int kGemmThreads = 384;
 constexpr int kEpiWarps = 8;
+constexpr int kEpiWarp0 = 4;                          // first promotion warp (warpgroups 1 and 2)
+// Register split: launched at 168 per thread (65536 / 384, rounded down to 8);
+// warpgroup 0 gives back to 40, the two promotion warpgroups take 232
+// (128 accumulators + 64 in-flight TMEM values + loop state, no spill):
+// 128 x 40 + 256 x 232 = 64512 = 384 x 168.
+constexpr uint32_t kRegsControl = 40;
+constexpr uint32_t kRegsEpilogue = 232;
+static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= 168u * kGemmThreads, "register split exceeds launch");
 constexpr int kUnitRing = 4;
 constexpr uint32_t kATileBytes = kGemmBM * kGemmBK;   // 16 KiB
 constexpr uint32_t kBTileBytes = kGemmBN * kGemmBK;   // 32 KiB
@@ -214,7 +225,7 @@ MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) 
   }
 }
 
-// Promotion + epilogue warps (warps 2..9).  Returns when the end marker arrives.
+// Promotion + epilogue warps (warps 4..11).  Returns when the end marker arrives.
 // `on_unit(m, e, rows)` lets the fused kernel acquire the tile's ready flag
 // before its first read of A_scale (always true for the unfused GEMM).
 template <typename OnUnit>
@@ -222,7 +233,7 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_uni
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                 // TMEM lane quarter this warp may access
-  const int h = (warp - 2) >> 2;          // column half: [h*128, h*128+128)
+  const int h = (warp - kEpiWarp0) >> 2;  // column half: [h*128, h*128+128)
   const int r_in_tile = q * 32 + lane;
   const int KB = g.H / kGemmBK;
   const int nsb = g.N / 128;
@@ -246,25 +257,22 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_uni
     float acc[128];
 #pragma unroll
     for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-    float sa_n = valid ? __ldcg(sa_ptr) : 0.0f;
-    float sb_n = __ldg(sb_ptr);
+    // block scales two K-blocks ahead (they come from L2)
+    float sa0 = valid ? __ldcg(sa_ptr) : 0.0f, sb0 = __ldg(sb_ptr);
+    float sa1 = (valid && KB > 1) ? __ldcg(sa_ptr + g.R) : 0.0f, sb1 = KB > 1 ? __ldg(sb_ptr + 1) : 0.0f;
     for (int kb = 0; kb < KB; ++kb) {
-      const float sc = sa_n * sb_n;
-      if (kb + 1 < KB) {
-        sa_n = valid ? __ldcg(sa_ptr + (size_t)(kb + 1) * g.R) : 0.0f;
-        sb_n = __ldg(sb_ptr + kb + 1);
+      const float sc = sa0 * sb0;
+      sa0 = sa1;
+      sb0 = sb1;
+      if (kb + 2 < KB) {
+        sa1 = valid ? __ldcg(sa_ptr + (size_t)(kb + 2) * g.R) : 0.0f;
+        sb1 = __ldg(sb_ptr + kb + 2);
       }
       const uint32_t p = pit & 1u, pph = (pit >> 1) & 1u;
       if (!mbar_wait(smem_u32(&sh->tfull[p]), pph, &sh->abort_flag, g.status, g.timeout_ns)) return;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + p * kGemmBN + h * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32_wait(taddr + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], sc, acc[c * 32 + i]);
-      }
+      tmem_fold128(taddr, sc, acc);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[p]));

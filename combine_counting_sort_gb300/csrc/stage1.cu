@@ -43,6 +43,8 @@ struct Stage1Params {
   int join;           // producers take GEMM work when done
   int use_tickets;
   int withhold_tile;  // test hook: rows of this tile are never published (-1: off)
+  int trace;          // record stamps / counters in the workspace header
+  unsigned long long* tr;  // trace slots
   int32_t* ticket;
   int32_t* qlen;
   int32_t* tile_flag;     // [max_tiles] rows landed
@@ -52,13 +54,20 @@ struct Stage1Params {
 
 // Bounded wait until the unit's rows have all landed; then order the later
 // async-proxy (TMA) reads after the acquired generic-proxy writes.
-MOE_DEV bool wait_ready(const Stage1Params& p, int m, int e, int rows, volatile int* abort_flag) {
+MOE_DEV bool wait_ready(const Stage1Params& p, int m, int e, int rows, volatile int* abort_flag,
+                        bool count = false) {
   const int32_t* flag = p.per_expert ? p.expert_flag + e : p.tile_flag + m;
   const int target = p.per_expert ? p.g.L.count[e] : rows;
   if (ld_acquire_gpu(flag) < target) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0;; ++i) {
-      if (ld_acquire_gpu(flag) >= target) break;
+      if (ld_acquire_gpu(flag) >= target) {
+        if (count && p.trace) {
+          atomicAdd(p.tr + MOE_TRACE_WAIT_NS, (unsigned long long)(globaltimer_ns() - t0));
+          atomicAdd(p.tr + MOE_TRACE_WAITED_UNITS, 1ull);
+        }
+        break;
+      }
       if ((i & 7u) == 7u) {
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > p.g.timeout_ns) {
@@ -194,6 +203,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int nbn = p.g.N / kGemmBN;
   const int KB = p.g.H / kGemmBK;
   const bool producer = (int)blockIdx.x < p.S;
+  if (p.trace && threadIdx.x == 0) atomicCAS(p.tr + MOE_TRACE_START, 0ull, (unsigned long long)globaltimer_ns());
 
   if (producer) {
     // the stage buffers are idle while producing: stage the expert offset tables there
@@ -218,6 +228,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // the stage buffers go back to the TMA (async proxy) after generic-proxy use
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
+    if (p.trace && threadIdx.x == 0) atomicMax(p.tr + MOE_TRACE_PRODUCED, (unsigned long long)globaltimer_ns());
     if (!p.join) {
       gemm_teardown(S);
       return;
@@ -225,8 +236,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   const int units = L.num_tiles[0] * nbn;
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp < kEpiWarp0) {
+    regs_dealloc<kRegsControl>();
+    if (warp == 0 && lane == 0) {
       uint32_t it = 0;
       int j = 0;
       bool ok = true;
@@ -238,23 +250,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (u < 0) break;
         const Unit x = unit_of(L, u, nbn);
         ok = publish_unit(S.sh, j, x, p.g.status, p.g.timeout_ns) &&
-             wait_ready(p, x.m, x.e, x.rows, &S.sh->abort_flag) &&
+             wait_ready(p, x.m, x.e, x.rows, &S.sh->abort_flag, true) &&
              produce_unit(S, &tmA, &tmW, x, KB, it, p.g.status, p.g.timeout_ns);
         ++j;
+      }
+      if (p.trace) {
+        atomicAdd(p.tr + MOE_TRACE_UNITS, (unsigned long long)j);
+        if (producer) atomicAdd(p.tr + MOE_TRACE_JOINED_UNITS, (unsigned long long)j);
       }
       if (ok) {
         Unit end = {-1, 0, 0, 0, 0};
         publish_unit(S.sh, j, end, p.g.status, p.g.timeout_ns);
       }
       drain_fills(S, it, p.g.timeout_ns);
+    } else if (warp == 1 && lane == 0) {
+      mma_loop(S, KB, p.g.status, p.g.timeout_ns);
     }
-  } else if (warp == 1) {
-    if (lane == 0) mma_loop(S, KB, p.g.status, p.g.timeout_ns);
   } else {
+    regs_alloc<kRegsEpilogue>();
     volatile int* ab = &S.sh->abort_flag;
     epilogue_loop(S, p.g, [&](int m, int e, int rows) { return wait_ready(p, m, e, rows, ab); });
   }
   gemm_teardown(S);
+  if (p.trace && threadIdx.x == 0) atomicMax(p.tr + MOE_TRACE_END, (unsigned long long)globaltimer_ns());
 }
 
 }  // namespace moe
@@ -315,6 +333,8 @@ extern "C" int moe_stage1(const uint16_t* x, int H, const moe_layout_t* L, const
   p.join = opts->producers_join != 0;
   p.use_tickets = p.join || p.ready_first;
   p.withhold_tile = opts->withhold_tile;
+  p.trace = opts->trace != 0;
+  p.tr = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + MOE_TRACE_OFFSET);
   char* base = reinterpret_cast<char*>(ws);
   p.ticket = reinterpret_cast<int32_t*>(base);
   p.qlen = p.ticket + 1;

@@ -196,8 +196,19 @@ typedef struct moe_stage1_opts {
   int64_t timeout_ns;        /* bound of every wait on a flag; 0 = default (1 s) */
   int32_t withhold_tile;     /* test hook: >= 0 never publishes this M-tile's rows (the
                                 consumer must time out); -1 = off */
-  int32_t reserved;
+  int32_t trace;             /* 1: record timestamps / wait counters in the workspace
+                                header (int64 slots MOE_TRACE_*, ns from %globaltimer) */
 } moe_stage1_opts_t;
+
+/* Trace slots (int64) of the stage1 workspace header when opts.trace = 1. */
+#define MOE_TRACE_OFFSET 64          /* byte offset of slot 0 in the workspace */
+#define MOE_TRACE_START 0            /* kernel start (first CTA to stamp) */
+#define MOE_TRACE_PRODUCED 1         /* last producer CTA done with its tokens */
+#define MOE_TRACE_WAIT_NS 2          /* total ns consumers spent waiting for ready flags */
+#define MOE_TRACE_WAITED_UNITS 3     /* units whose first load had to wait */
+#define MOE_TRACE_END 4              /* last CTA done */
+#define MOE_TRACE_JOINED_UNITS 5     /* units taken by producer CTAs after joining */
+#define MOE_TRACE_UNITS 6            /* units processed in total */
 
 /*   x, H, L        as moe_dispatch_quant; W, W_scale, N as moe_grouped_gemm1.
  *   A, A_scale, Y  outputs as the unfused calls.
