@@ -126,6 +126,18 @@ MOE_DEV uint16_t bf16_of_product(float a, float b) {
 
 // ---------------------------------------------------------------- shared memory / mbarrier
 
+// One lane of a converged warp (elect.sync): tcgen05 / TMA issue from a
+// warp whose other lanes run the same (warp-uniform) loop.
+MOE_DEV bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 MOE_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 MOE_DEV void mbar_init(uint32_t bar, uint32_t count) {

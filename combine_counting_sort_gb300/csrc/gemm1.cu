@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp < kEpiWarp0) {
     regs_dealloc<kRegsControl>();
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
       uint32_t it = 0;
       int j = 0;
       bool ok = true;
@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         publish_unit(S.sh, j, end, g.status, g.timeout_ns);
       }
       drain_fills(S, it, g.timeout_ns);
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       mma_loop(S, KB, g.status, g.timeout_ns);
     }
   } else {

@@ -72,7 +72,14 @@ struct GemmShared {
   int abort_flag;
 };
 
-constexpr size_t kGemmSmemBytes = 1024 + (size_t)kGemmStages * kStageBytes + sizeof(GemmShared);
+// Output staging: 4 KB per promotion warp (32 rows x 64 bf16 columns, 16-byte
+// chunks XOR-swizzled by row) so that the Y store goes out in full 128-byte
+// row segments.
+constexpr uint32_t kOutStageBytes = 32 * 64 * 2;
+constexpr size_t kGemmSmemBytes =
+    1024 + (size_t)kGemmStages * kStageBytes + ((sizeof(GemmShared) + 127) & ~size_t(127)) +
+    (size_t)kEpiWarps * kOutStageBytes;
+static_assert(kGemmSmemBytes <= 232448, "shared memory budget of one CTA");
 
 struct GemmParams {
   const float* A_scale;   // [H/128][R]
@@ -89,6 +96,7 @@ struct GemmParams {
 struct GemmSmem {
   uint8_t* stages;
   GemmShared* sh;
+  uint8_t* out_stage;   // kEpiWarps x kOutStageBytes
 };
 
 MOE_DEV GemmSmem gemm_smem(uint8_t* raw) {
@@ -97,6 +105,7 @@ MOE_DEV GemmSmem gemm_smem(uint8_t* raw) {
   GemmSmem g;
   g.stages = raw + pad;
   g.sh = reinterpret_cast<GemmShared*>(g.stages + (size_t)kGemmStages * kStageBytes);
+  g.out_stage = reinterpret_cast<uint8_t*>(g.sh) + ((sizeof(GemmShared) + 127) & ~size_t(127));
   return g;
 }
 
@@ -145,18 +154,23 @@ struct Unit {
   int m, nb, e, row0, rows;
 };
 
-// Producer side: publish unit j (m < 0 = end of work) into the ring.
+// Producer warp (all 32 lanes, converged; one elected lane writes and issues):
+// publish unit j (m < 0 = end of work) into the ring.
 MOE_DEV bool publish_unit(GemmShared* sh, int j, const Unit& u, int32_t* status, uint64_t tmo) {
   const int slot = j % kUnitRing;
   const uint32_t ph = (uint32_t)(j / kUnitRing) & 1u;
   if (!mbar_wait(smem_u32(&sh->uempty[slot]), ph ^ 1u, &sh->abort_flag, status, tmo)) return false;
-  sh->unit[slot] = make_int4(u.m, u.nb, u.e, u.row0);
-  sh->unit_rows[slot] = u.rows;
-  mbar_arrive(smem_u32(&sh->ufull[slot]));
+  if (elect_one()) {
+    sh->unit[slot] = make_int4(u.m, u.nb, u.e, u.row0);
+    sh->unit_rows[slot] = u.rows;
+    mbar_arrive(smem_u32(&sh->ufull[slot]));
+  }
+  __syncwarp();
   return true;
 }
 
-// Stream the K-blocks of one unit into the stage ring.  `it` counts stage fills.
+// Producer warp: stream the K-blocks of one unit into the stage ring.  `it`
+// counts stage fills.
 MOE_DEV bool produce_unit(const GemmSmem& S, const CUtensorMap* tmA, const CUtensorMap* tmW,
                           const Unit& u, int KB, uint32_t& it, int32_t* status, uint64_t tmo) {
   GemmShared* sh = S.sh;
@@ -164,11 +178,14 @@ MOE_DEV bool produce_unit(const GemmSmem& S, const CUtensorMap* tmA, const CUten
     const int s = (int)(it % kGemmStages);
     const uint32_t ph = (it / kGemmStages) & 1u;
     if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, &sh->abort_flag, status, tmo)) return false;
-    const uint32_t full = smem_u32(&sh->full[s]);
-    mbar_arrive_expect_tx(full, kStageBytes);
-    const uint32_t dstA = smem_u32(S.stages + (size_t)s * kStageBytes);
-    tma_load_2d(dstA, tmA, kb * kGemmBK, u.row0, full);
-    tma_load_3d(dstA + kATileBytes, tmW, kb * kGemmBK, u.nb * kGemmBN, u.e, full);
+    if (elect_one()) {
+      const uint32_t full = smem_u32(&sh->full[s]);
+      mbar_arrive_expect_tx(full, kStageBytes);
+      const uint32_t dstA = smem_u32(S.stages + (size_t)s * kStageBytes);
+      tma_load_2d(dstA, tmA, kb * kGemmBK, u.row0, full);
+      tma_load_3d(dstA + kATileBytes, tmW, kb * kGemmBK, u.nb * kGemmBN, u.e, full);
+    }
+    __syncwarp();
     ++it;
   }
   return true;
@@ -182,7 +199,9 @@ MOE_DEV void drain_fills(const GemmSmem& S, uint32_t it, uint64_t tmo) {
     mbar_wait(smem_u32(&S.sh->full[i % kGemmStages]), (i / kGemmStages) & 1u, &dummy_abort, nullptr, tmo);
 }
 
-// MMA thread: consume units until the end marker.
+// MMA warp (all 32 lanes run the loop; one elected lane issues the tcgen05
+// instructions, so descriptors and addresses stay warp-uniform): consume units
+// until the end marker.
 MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) {
   GemmShared* sh = S.sh;
   const uint32_t tmem = sh->tmem_base;
@@ -193,7 +212,8 @@ MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) 
     if (!mbar_wait(smem_u32(&sh->ufull[slot]), (uint32_t)(j / kUnitRing) & 1u, &sh->abort_flag, status, tmo))
       break;
     const int m = sh->unit[slot].x;
-    mbar_arrive(smem_u32(&sh->uempty[slot]));
+    __syncwarp();
+    if (elect_one()) mbar_arrive(smem_u32(&sh->uempty[slot]));
     if (m < 0) break;
     bool ok = true;
     for (int kb = 0; kb < KB && ok; ++kb) {
@@ -206,12 +226,16 @@ MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) 
       tc_fence_after();
       const uint32_t a0 = smem_u32(S.stages + (size_t)s * kStageBytes);
       const uint32_t b0 = a0 + kATileBytes;
+      if (elect_one()) {
 #pragma unroll
-      for (int k4 = 0; k4 < kGemmBK / 32; ++k4)
-        umma_f8f6f4(tmem + p * kGemmBN, sw128_kmajor_desc(a0 + k4 * 32), sw128_kmajor_desc(b0 + k4 * 32),
-                    kIdesc, k4 > 0 ? 1u : 0u);
-      umma_commit(smem_u32(&sh->empty[s]));
-      umma_commit(smem_u32(&sh->tfull[p]));
+        for (int k4 = 0; k4 < kGemmBK / 32; ++k4)
+          umma_f8f6f4(tmem + p * kGemmBN, sw128_kmajor_desc(a0 + k4 * 32), sw128_kmajor_desc(b0 + k4 * 32),
+                      kIdesc, k4 > 0 ? 1u : 0u);
+        // one commit per K-block: the promotion warps release the smem stage
+        // (empty[s]) when they see the partial, i.e. when these MMAs are done
+        umma_commit(smem_u32(&sh->tfull[p]));
+      }
+      __syncwarp();
       issued = true;
       ++it;
       ++pit;
@@ -220,7 +244,8 @@ MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) 
   }
   if (issued) {   // no MMA may be in flight when TMEM is freed
     int dummy_abort = 0;
-    umma_commit(smem_u32(&sh->drain));
+    if (elect_one()) umma_commit(smem_u32(&sh->drain));
+    __syncwarp();
     mbar_wait(smem_u32(&sh->drain), 0u, &dummy_abort, nullptr, tmo);
   }
 }
@@ -270,6 +295,8 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_uni
       }
       const uint32_t p = pit & 1u, pph = (pit >> 1) & 1u;
       if (!mbar_wait(smem_u32(&sh->tfull[p]), pph, &sh->abort_flag, g.status, g.timeout_ns)) return;
+      // the MMAs that read smem stage (pit % stages) are complete: hand the stage back to the TMA thread
+      if (warp == kEpiWarp0 && lane == 0) mbar_arrive(smem_u32(&sh->empty[pit % kGemmStages]));
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + p * kGemmBN + h * 128;
       tmem_fold128(taddr, sc, acc);
@@ -278,17 +305,36 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_uni
       if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[p]));
       ++pit;
     }
-    if (valid) {
-      uint4* dst = reinterpret_cast<uint4*>(g.Y + (size_t)(row0 + r_in_tile) * g.N + (size_t)nb * kGemmBN + h * 128);
+    // bf16 output through the warp's staging tile: lane = row on the way in,
+    // 8 lanes per row (4 rows per instruction) on the way out
+    uint8_t* stg = S.out_stage + (size_t)(warp - kEpiWarp0) * kOutStageBytes;
+    const uint32_t stg_s = smem_u32(stg);
+    uint16_t* ybase = g.Y + (size_t)row0 * g.N + (size_t)nb * kGemmBN + h * 128;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        uint4 o;
-        o.x = pack_bf16x2(acc[8 * c + 0], acc[8 * c + 1]);
-        o.y = pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]);
-        o.z = pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]);
-        o.w = pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]);
-        dst[c] = o;
+    for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int a = pass * 64 + c * 8;
+        const uint32_t dst = stg_s + lane * 128 + ((c ^ (lane & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                     "r"(pack_bf16x2(acc[a + 0], acc[a + 1])), "r"(pack_bf16x2(acc[a + 2], acc[a + 3])),
+                     "r"(pack_bf16x2(acc[a + 4], acc[a + 5])), "r"(pack_bf16x2(acc[a + 6], acc[a + 7]))
+                     : "memory");
       }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int row = i * 4 + (lane >> 3), chunk = lane & 7;
+        uint4 v;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(stg_s + row * 128 + ((chunk ^ (row & 7)) << 4))
+                     : "memory");
+        const int r = q * 32 + row;
+        if (r < rows)
+          *reinterpret_cast<uint4*>(ybase + (size_t)r * g.N + pass * 64 + chunk * 8) = v;
+      }
+      __syncwarp();
     }
   }
 }

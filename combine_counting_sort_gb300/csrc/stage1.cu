@@ -238,23 +238,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int units = L.num_tiles[0] * nbn;
   if (warp < kEpiWarp0) {
     regs_dealloc<kRegsControl>();
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
+      // the whole warp runs the loop (converged, warp-uniform values); lane 0
+      // claims units (ticket atomics, queue reads) and broadcasts them
       uint32_t it = 0;
       int j = 0;
       bool ok = true;
       int cursor = (int)blockIdx.x - p.S;
       const int stride = (int)gridDim.x - p.S;
       while (ok) {
-        const int u = next_unit(p, units, nbn, cursor, stride, &S.sh->abort_flag);
+        int u = 0;
+        if (lane == 0) u = next_unit(p, units, nbn, cursor, stride, &S.sh->abort_flag);
+        u = __shfl_sync(0xffffffffu, u, 0);
         if (u == -2) { ok = false; break; }
         if (u < 0) break;
         const Unit x = unit_of(L, u, nbn);
         ok = publish_unit(S.sh, j, x, p.g.status, p.g.timeout_ns) &&
-             wait_ready(p, x.m, x.e, x.rows, &S.sh->abort_flag, true) &&
+             wait_ready(p, x.m, x.e, x.rows, &S.sh->abort_flag, lane == 0) &&
              produce_unit(S, &tmA, &tmW, x, KB, it, p.g.status, p.g.timeout_ns);
         ++j;
       }
-      if (p.trace) {
+      if (p.trace && lane == 0) {
         atomicAdd(p.tr + MOE_TRACE_UNITS, (unsigned long long)j);
         if (producer) atomicAdd(p.tr + MOE_TRACE_JOINED_UNITS, (unsigned long long)j);
       }
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         publish_unit(S.sh, j, end, p.g.status, p.g.timeout_ns);
       }
       drain_fills(S, it, p.g.timeout_ns);
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       mma_loop(S, KB, p.g.status, p.g.timeout_ns);
     }
   } else {
