@@ -23,14 +23,40 @@ MOE_DEV void unpack16(const uint4& a, const uint4& b, float (&f)[16]) {
 }
 
 // 16 values of one quantisation block (this lane's share) -> 16 e4m3 codes:
-// code = e4m3_rn_satfinite(x / scale) with IEEE fp32 division; scale 0 -> codes 0.
+// code = e4m3_rn_satfinite(RN(x / scale)) with the IEEE fp32 quotient; scale 0
+// -> codes 0.
+//
+// Fast path: v' = RN(x * RN(1/scale)).  Both roundings are relative errors of
+// at most 2^-24, so v' is within 3 fp32 ulps of the exact quotient RN(x/scale),
+// and both lie on the same side of every e4m3 rounding boundary unless v' is
+// within 4 ulps of one.  In the e4m3 normal range those boundaries (midpoints
+// between adjacent codes) are exactly the fp32 values whose low 20 mantissa
+// bits are 0x80000; binade edges are codes, not boundaries.  So v' gives the
+// same code as the quotient unless its low 20 bits are within 4 of 0x80000 or
+// it lies below 2^-6 (the e4m3 subnormal range); a lane holding any such value
+// recomputes its 16 values with the IEEE division.
 MOE_DEV uint4 quant16(const float (&f)[16], float scale) {
   uint32_t p[4] = {0u, 0u, 0u, 0u};
   if (scale > 0.0f) {
+    const float inv = __frcp_rn(scale);
+    float v[16];
+    bool slow = false;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      v[i] = __fmul_rn(f[i], inv);
+      const uint32_t u = __float_as_uint(v[i]);
+      const uint32_t e = (u >> 23) & 0xFFu;
+      const uint32_t d = (u & 0xFFFFFu) - 0x80000u;
+      slow |= (e < 121u) | ((d + 4u) <= 8u);     // below 2^-6, or near a midpoint
+    }
+    if (slow) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = __fdiv_rn(f[i], scale);
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = e4m3x2(__fdiv_rn(f[4 * i + 0], scale), __fdiv_rn(f[4 * i + 1], scale));
-      const uint32_t hi = e4m3x2(__fdiv_rn(f[4 * i + 2], scale), __fdiv_rn(f[4 * i + 3], scale));
+      const uint32_t lo = e4m3x2(v[4 * i + 0], v[4 * i + 1]);
+      const uint32_t hi = e4m3x2(v[4 * i + 2], v[4 * i + 3]);
       p[i] = lo | (hi << 16);
     }
   }

@@ -136,3 +136,42 @@ def test_combine_random_matches_oracle(T, k, D):
     moe.moe_combine(Y, L2, out, status)
     torch.cuda.synchronize()
     assert np.array_equal(gu.bits(out), oracle.combine(Yb, L2["pair_row"].cpu().numpy(), onehot))
+
+
+def test_dispatch_every_bf16_quotient_bit_exact():
+    # For block maxima a (random bf16 values plus awkward ones), quantise every
+    # bf16 value |x| <= a in blocks whose maximum is a: every quotient x/scale the
+    # format can produce, including those closest to the e4m3 rounding midpoints.
+    rng = np.random.default_rng(11)
+    amaxes = list(oracle.bf16_to_f32(rng.integers(0x3C00, 0x4600, 24).astype(np.uint16)))
+    amaxes += [1.0, 3.0, 448.0, 0.1, 7.0 / 3.0, 1e-3, 1e4]
+    blocks = []
+    for a in amaxes:
+        ab = oracle.f64_to_bf16(np.array([a]))[0]
+        a = float(oracle.bf16_to_f32(np.array([ab]))[0])
+        pos = np.arange(0, int(ab) + 1, dtype=np.uint32).astype(np.uint16)      # every bf16 in [0, a]
+        vals = np.concatenate([pos, pos | np.uint16(0x8000)])
+        rng.shuffle(vals)
+        per = 127
+        nblk = (len(vals) + per - 1) // per
+        vals = np.concatenate([vals, np.zeros(nblk * per - len(vals), np.uint16)]).reshape(nblk, per)
+        blocks.append(np.concatenate([np.full((nblk, 1), ab, np.uint16), vals], axis=1))   # max = a
+    allb = np.concatenate(blocks)
+    H, k, E, G = 1024, 1, 4, 1
+    per_tok = H // 128
+    T = (len(allb) + per_tok - 1) // per_tok
+    allb = np.concatenate([allb, np.zeros((T * per_tok - len(allb), 128), np.uint16)])
+    xb = allb.reshape(T, H)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16)
+    ids = (np.arange(T) % E).astype(np.int32)[:, None]
+    w = np.ones((T, k), np.float32)
+    L, status = gu.gpu_layout(ids, w, E, G)
+    R = T * k
+    A = torch.empty((R, H), dtype=torch.uint8, device="cuda")
+    As = torch.empty((H // 128, R), dtype=torch.float32, device="cuda")
+    moe.moe_dispatch_quant(x.cuda(), L, A, As, status)
+    torch.cuda.synchronize()
+    q, s = oracle.quantize_rows(xb)
+    A_ref, As_ref = oracle.dispatch(q, s, L["pair_row"].cpu().numpy(), k)
+    assert np.array_equal(A.cpu().numpy(), A_ref)
+    assert np.array_equal(As.cpu().numpy().view(np.uint32), As_ref.view(np.uint32))
