@@ -33,6 +33,24 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "stage1 µs & tokens/s at T=8192 (GEMM1 TFLOP/s); dispatch/combine HBM GB/s"
+
+# DRAM bytes per launch of the roofline kernel (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# single-pass ncu capture of the full workload, keyed by workload, stage1 variant and a hash of the
+# kernel sources the capture ran on.  A kernel changed since then reports null until captured again.
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum \
+#       --clock-control none -k regex:stage1_kernel -s 3 -c 1 \
+#       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-clocks
+KERNEL_SOURCES = ["common.cuh", "gemm1.cuh", "quant.cuh", "stage1.cu", "tmem_fold.cuh"]
+TRAFFIC = {("t8192_zipf1.2", "fused/comm36/per_tile/expert_major/join1", "6bbaefa6432fc4b4"): 6.73e9}
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha1()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "combine_counting_sort_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2
 FP8_OVER_BF16 = 2.0                 # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
@@ -258,6 +276,10 @@ def run_gpu(args):
     peaks = measured_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     stage_avg = statistics.mean(stage_ms) if fused else u_gemm
+    variant_key = "%s/comm%d/%s/%s/join%d" % (args.variant, args.comm_sms, ["per_tile", "per_expert"][args.flags],
+                                              ["expert_major", "ready_first"][args.schedule], args.join)
+    traffic = args.traffic if args.traffic is not None else \
+        TRAFFIC.get((cfg.name, variant_key, kernel_source_hash()))
     achieved = wl.gemm_flops() / (stage_avg / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -275,7 +297,9 @@ def run_gpu(args):
                      "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / fp8_peak, 4),
                      "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (fp8/bf16 nominal)",
-                     "traffic": args.traffic},
+                     "traffic": traffic,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one full-size launch"
+                     if traffic is not None else None},
         "stage1_us": round(statistics.median(stage_ms) * 1e3, 1),
         "layout_us": round(statistics.median(layout_ms) * 1e3, 1),
         "combine_us": round(statistics.median(comb_ms) * 1e3, 1),
@@ -444,7 +468,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="t8192_zipf1.2")
     ap.add_argument("--variant", choices=["fused", "unfused"], default="fused")
-    ap.add_argument("--comm-sms", type=int, default=16)
+    ap.add_argument("--comm-sms", type=int, default=36)
     ap.add_argument("--flags", type=int, default=0, help="0 per-tile, 1 per-expert")
     ap.add_argument("--schedule", type=int, default=0, help="0 expert-major, 1 ready-first")
     ap.add_argument("--join", type=int, default=1, help="producer CTAs take GEMM work when done")
