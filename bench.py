@@ -460,6 +460,98 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- sweeps (one JSON line per case)
+
+def _time_events(fn, s, reps, flush):
+    ts = []
+    for i in range(reps + 2):
+        if flush is not None:
+            with torch.cuda.stream(s):
+                flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        if i >= 2:
+            ts.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(ts)
+
+
+def run_bw_sweep(args):
+    """Dispatch + combine with the identity expert (no GEMM): GB/s per kernel vs HBM."""
+    import combine_counting_sort_gb300 as moe
+    from combine_counting_sort_gb300 import inputs
+    import __graft_entry__ as ge
+    ge.build()
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peak = measured_peaks()["hbm_gbs"]
+    for T in (2048, 4096, 8192, 16384):
+        cfg = inputs.CONFIGS[f"bw_t{T}"]
+        x = inputs.make_x(T, cfg.H, cfg.seed).to(dev)
+        logits = inputs.make_logits(T, cfg.E, cfg.zipf, cfg.seed).to(dev)
+        ids = torch.empty(T, cfg.k, dtype=torch.int32, device=dev)
+        w = torch.empty(T, cfg.k, dtype=torch.float32, device=dev)
+        moe.moe_router_topk(logits, cfg.k, ids, w)
+        L = moe.Layout(T, cfg.k, cfg.E, cfg.G, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        moe.moe_route_layout(ids, w, L, st)
+        R = T * cfg.k
+        A = torch.empty(R, cfg.H, dtype=torch.uint8, device=dev)
+        As = torch.empty(cfg.H // 128, R, dtype=torch.float32, device=dev)
+        Y = torch.empty(R, cfg.H, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
+        lay = _time_events(lambda: moe.moe_route_layout(ids, w, L, st, stream=s), s, args.steps, flush)
+        d_us = _time_events(lambda: moe.moe_dispatch_quant(x, L, A, As, st, stream=s), s, args.steps, flush)
+        moe.moe_dequant_rows(A, As, L, Y, stream=s)
+        c_us = _time_events(lambda: moe.moe_combine(Y, L, out, st, stream=s), s, args.steps, flush)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        d_bytes = 2.0 * T * cfg.H + R * cfg.H + 4.0 * R * cfg.H / 128
+        c_bytes = 2.0 * R * cfg.H + 2.0 * T * cfg.H + 8.0 * R
+        print(json.dumps({"sweep": "dispatch_combine_bw", "T": T, "H": cfg.H, "E": cfg.E, "k": cfg.k,
+                          "layout_us": round(lay, 1), "dispatch_us": round(d_us, 1),
+                          "dispatch_gbs": round(d_bytes / d_us / 1e3, 1), "dispatch_frac": round(d_bytes / d_us / 1e3 / peak, 3),
+                          "combine_us": round(c_us, 1), "combine_gbs": round(c_bytes / c_us / 1e3, 1),
+                          "combine_frac": round(c_bytes / c_us / 1e3 / peak, 3), "hbm_peak_gbs": peak}), flush=True)
+        del x, A, As, Y, out, L
+
+
+def run_stage1_sweep(args):
+    """Fused stage1 at T=16384 Zipf(1.0): producer SMs x flag granularity x schedule vs the unfused sum."""
+    import combine_counting_sort_gb300 as moe
+    from combine_counting_sort_gb300 import inputs
+    import __graft_entry__ as ge
+    ge.build()
+    dev = torch.device("cuda", 0)
+    cfg = inputs.CONFIGS["stage1_t16384_zipf1.0"]
+    wl = Workload(cfg, dev, moe.stage1_opts())
+    s = torch.cuda.Stream(dev)
+    moe.moe_route_layout(wl.ids, wl.w, wl.L, wl.status, stream=s)
+    disp = _time_events(lambda: moe.moe_dispatch_quant(wl.x, wl.L, wl.A, wl.As, wl.status, stream=s), s,
+                        args.steps, wl.flush)
+    gemm = _time_events(lambda: moe.moe_grouped_gemm1(wl.A, wl.As, wl.Wq, wl.Ws, wl.L, wl.Y, wl.status, stream=s),
+                        s, args.steps, wl.flush)
+    print(json.dumps({"sweep": "stage1", "workload": cfg.name, "variant": "unfused", "dispatch_us": round(disp, 1),
+                      "gemm1_us": round(gemm, 1), "sum_us": round(disp + gemm, 1)}), flush=True)
+    for comm in (8, 16, 24, 36):
+        for flags in (moe.MOE_FLAGS_PER_TILE, moe.MOE_FLAGS_PER_EXPERT):
+            for sched in (moe.MOE_SCHED_EXPERT_MAJOR, moe.MOE_SCHED_READY_FIRST):
+                opts = moe.stage1_opts(comm_sms=comm, flags=flags, schedule=sched, trace=1)
+                us = _time_events(lambda: moe.moe_stage1(wl.x, wl.L, wl.Wq, wl.Ws, wl.A, wl.As, wl.Y, wl.ws,
+                                                         wl.status, opts, stream=s), s, args.steps, wl.flush)
+                tr = moe.stage1_trace(wl.ws)
+                print(json.dumps({"sweep": "stage1", "workload": cfg.name, "comm_sms": comm,
+                                  "flags": ["per_tile", "per_expert"][flags],
+                                  "schedule": ["expert_major", "ready_first"][sched], "stage1_us": round(us, 1),
+                                  "vs_unfused_sum": round(us / (disp + gemm), 3),
+                                  "produced_us": round(tr["produced_us"], 1),
+                                  "consumer_wait_us_total": round(tr["wait_us_total"], 1)}), flush=True)
+    assert wl.status.item() == 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,11 +569,18 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--sweep", choices=["bw", "stage1"], default=None,
+                    help="instead of the bench line: the dispatch/combine bandwidth sweep (identity expert, "
+                         "T=2048..16384) or the fused stage1 sweep (T=16384 Zipf 1.0), one JSON line per case")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep == "bw":
+        run_bw_sweep(args)
+    elif args.sweep == "stage1":
+        run_stage1_sweep(args)
     else:
         run_gpu(args)
 

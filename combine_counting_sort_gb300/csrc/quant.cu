@@ -8,15 +8,29 @@ namespace moe {
 
 constexpr int kQuantWarps = 8;
 
-__global__ void __launch_bounds__(kQuantWarps * 32) dispatch_quant_kernel(
-    const uint16_t* __restrict__ x, int H, LayoutDev L, uint8_t* __restrict__ A,
+// One warp per (token, column range) work item: a token's H columns are split
+// into `splits` ranges of whole chunks of ROUNDS x 512 columns (the mori page's
+// --split), as many as it takes to give every SM enough warps; each item walks
+// its range chunk by chunk.  Batches below 8192 tokens use 1024-column chunks
+// (more items), larger ones 2048-column chunks (4 KB of the row in flight per warp).
+template <int ROUNDS>
+__global__ void __launch_bounds__(kQuantWarps * 32, ROUNDS == 2 ? 4 : 3) dispatch_quant_kernel(
+    const uint16_t* __restrict__ x, int H, LayoutDev L, int splits, uint8_t* __restrict__ A,
     float* __restrict__ A_scale) {
+  constexpr int kSliceCols = 512 * ROUNDS;
   const int lane = threadIdx.x & 31;
   const int T = L.T, k = L.k;
   const long long R = (long long)T * k;
-  for (int t = blockIdx.x * kQuantWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kQuantWarps) {
+  const int chunks = (H + kSliceCols - 1) / kSliceCols;
+  const int per = (chunks + splits - 1) / splits;
+  const long long items = (long long)T * splits;
+  for (long long w = (long long)blockIdx.x * kQuantWarps + (threadIdx.x >> 5); w < items;
+       w += (long long)gridDim.x * kQuantWarps) {
+    const int t = (int)(w / splits), sp = (int)(w % splits);
     const int myrow = lane < k ? L.pair_row[(size_t)t * k + lane] : -1;
-    quant_scatter_token(x, H, t, k, R, myrow, A, A_scale);
+    const int cend = min(chunks, (sp + 1) * per);
+    for (int c = sp * per; c < cend; ++c)
+      quant_scatter_slice<ROUNDS>(x, H, t, c * kSliceCols, k, R, myrow, A, A_scale);
   }
 }
 
@@ -100,9 +114,19 @@ extern "C" int moe_dispatch_quant(const uint16_t* x, int H, const moe_layout_t* 
   if (!aligned16(x) || !aligned16(A) || !aligned16(A_scale)) return MOE_ERR_INVALID_ARG;
   const int nsm = device_sm_count();
   if (nsm <= 0) return MOE_ERR_CUDA;
-  const int blocks = std::max(1, std::min((L->T + kQuantWarps - 1) / kQuantWarps, nsm * 8));
-  dispatch_quant_kernel<<<blocks, kQuantWarps * 32, 0, (cudaStream_t)stream>>>(x, H, to_dev(L), A,
-                                                                               A_scale);
+  // small batches: every 1024-column chunk is an item; large ones: split tokens
+  // only as far as needed for ~64 warps per SM
+  const bool small = L->T < 8192;
+  const int cols = small ? 1024 : 2048;
+  const int chunks = (H + cols - 1) / cols;
+  const long long want = (long long)nsm * 64;
+  const int splits = small ? chunks : (int)std::max(1LL, std::min((long long)chunks, (want + L->T - 1) / L->T));
+  const long long items = (long long)L->T * splits;
+  const int blocks = (int)std::max(1LL, std::min((items + kQuantWarps - 1) / kQuantWarps, (long long)nsm * 16));
+  if (small)
+    dispatch_quant_kernel<2><<<blocks, kQuantWarps * 32, 0, (cudaStream_t)stream>>>(x, H, to_dev(L), splits, A, A_scale);
+  else
+    dispatch_quant_kernel<4><<<blocks, kQuantWarps * 32, 0, (cudaStream_t)stream>>>(x, H, to_dev(L), splits, A, A_scale);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

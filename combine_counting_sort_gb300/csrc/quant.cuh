@@ -74,6 +74,51 @@ MOE_DEV float block_amax8(const float (&f)[16]) {
   return am;
 }
 
+// One slice [c0, c0 + 512*ROUNDS) of token t (the mori page's --split: a
+// token's hidden dimension shared by several warps): all 2*ROUNDS 16-byte
+// loads of the lane are issued before any arithmetic, so each warp keeps
+// ROUNDS KB of the row in flight; then the 512-column rounds are quantised
+// and stored to the token's k rows.  `myrow` as in quant_scatter_token.
+template <int ROUNDS>
+MOE_DEV void quant_scatter_slice(const uint16_t* __restrict__ x, int H, int t, int c0, int k, long long R,
+                                 int myrow, uint8_t* __restrict__ A, float* __restrict__ A_scale) {
+  const int lane = threadIdx.x & 31;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  uint4 raw[2 * ROUNDS];
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    const int col = c0 + r * 512 + lane * 16;
+    raw[2 * r] = make_uint4(0, 0, 0, 0);
+    raw[2 * r + 1] = raw[2 * r];
+    if (col < H) {
+      raw[2 * r] = __ldcs(xr + col / 8);
+      raw[2 * r + 1] = __ldcs(xr + col / 8 + 1);
+    }
+  }
+  uint4 q[ROUNDS];
+  float sc[ROUNDS];
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    float f[16];
+    unpack16(raw[2 * r], raw[2 * r + 1], f);
+    sc[r] = __fdiv_rn(block_amax8(f), 448.0f);
+    q[r] = quant16(f, sc[r]);
+  }
+  for (int j = 0; j < k; ++j) {
+    const int row = __shfl_sync(0xffffffffu, myrow, j);
+    if (row < 0) continue;
+    uint8_t* arow = A + (size_t)row * H;
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+      const int col = c0 + r * 512 + lane * 16;
+      if (col < H) {
+        *reinterpret_cast<uint4*>(arow + col) = q[r];
+        if ((lane & 7) == 0) A_scale[(size_t)(col / kQBlock) * R + row] = sc[r];
+      }
+    }
+  }
+}
+
 // Quantise token t once (scale = amax/448 per 128 values) and store codes and
 // scales to each of its k rows; `myrow` is pair_row[t*k + lane] for lanes < k
 // (-1 elsewhere / for skipped pairs).  Whole warp, converged.
