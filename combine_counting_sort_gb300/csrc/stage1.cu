@@ -91,7 +91,8 @@ MOE_DEV void produce_tokens(const Stage1Params& p, int gw, int PW, const int* s_
   for (int i = gw; i < T; i += PW) {
     const int t = L.token_order[i];
     const int myrow = lane < k ? L.pair_row[(size_t)t * k + lane] : -1;
-    quant_scatter_token(p.x, p.g.H, t, k, p.g.R, myrow, p.A, p.A_scale);
+    for (int c0 = 0; c0 < p.g.H; c0 += 2048)     // 2048-column chunks: 4 KB of the row in flight
+      quant_scatter_slice<4>(p.x, p.g.H, t, c0, k, p.g.R, myrow, p.A, p.A_scale);
     fence_proxy_async_global();
     __syncwarp();
     if (myrow >= 0) {
