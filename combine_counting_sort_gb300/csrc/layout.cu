@@ -10,12 +10,15 @@
 //            pairs and first (smallest) experts of its tokens, with
 //            warp-aggregated shared-memory adds (__match_any_sync leaders);
 //            the block's ids and weights stay staged in shared memory.
-//   barrier  one grid-wide barrier (bounded spin).
-//   phase B  every block scans the per-block histograms down its own column
-//            (its exclusive prefix per expert) and across experts (expert
-//            offsets, tile offsets, first-expert offsets) in shared memory;
-//            block 0 writes the E-sized tables, all blocks write tile tables
-//            and the rowmap grid-stride.
+//   barrier  grid-wide barrier (bounded spin).
+//   phase B  the per-block histograms are scanned down the blocks, one warp
+//            per expert column (in place: each entry becomes that block's
+//            exclusive prefix; the column total goes to a totals array);
+//            after a second grid barrier every block reads its own row of
+//            prefixes and the totals, scans across experts (expert offsets,
+//            tile offsets, first-expert offsets) in shared memory; block 0
+//            writes the E-sized tables, all blocks write tile tables and the
+//            rowmap grid-stride.
 //   phase C  stable ranks: warp 0 walks the block's pairs in (token, slot)
 //            order 32 at a time; lanes with equal experts find each other with
 //            __match_any_sync and take consecutive rows; warp 1 does the same
@@ -39,7 +42,8 @@ struct LayoutArgs {
   LayoutDev L;
   int32_t* ws_hist;     // [nblk][E]
   int32_t* ws_fhist;    // [nblk][E]
-  uint32_t* ws_barrier; // zeroed in-stream before the launch
+  int32_t* ws_tot;      // [2][E] column totals of ws_hist / ws_fhist
+  uint32_t* ws_barrier; // [2] zeroed in-stream before the launch
   int32_t* status;
   int tpb;              // tokens per block
   uint64_t timeout_ns;
@@ -52,6 +56,62 @@ __device__ __forceinline__ int first_expert(const int32_t* s_ids, int k, int E) 
     if (e >= 0 && e < E && e < fe) fe = e;
   }
   return fe;
+}
+
+// Grid-wide barrier on counter `ctr` (all blocks co-resident: cooperative
+// launch), bounded by timeout_ns; false (and MOE_ERR_TIMEOUT) if it gave up.
+// `flag` is a shared int used to broadcast the outcome.
+__device__ bool grid_barrier(uint32_t* ctr, int nblk, int32_t* status, uint64_t timeout_ns, int* flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int timed_out = 0;
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    const uint64_t tstart = globaltimer_ns();
+    while (true) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+      if (v >= (unsigned)nblk) break;
+      if (globaltimer_ns() - tstart > timeout_ns) {
+        set_status(status, MOE_ERR_TIMEOUT);
+        timed_out = 1;
+        break;
+      }
+      __nanosleep(64);
+    }
+    *flag = timed_out;
+  }
+  __syncthreads();
+  return *flag == 0;
+}
+
+// One warp scans column `col` (stride E, nblk <= 256 entries) in place into
+// exclusive prefixes and returns the column total (all lanes).
+__device__ int warp_column_scan(int32_t* col, int E, int nblk) {
+  const int lane = threadIdx.x & 31;
+  const int per = (nblk + 31) / 32;     // <= 8
+  int v[8];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int bb = lane * per + i;
+    v[i] = (i < per && bb < nblk) ? __ldcg(col + (size_t)bb * E) : 0;
+    sum += v[i];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  int run = incl - sum;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int bb = lane * per + i;
+    if (i < per && bb < nblk) col[(size_t)bb * E] = run;
+    run += v[i];
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
 }
 
 // Exclusive scan over n <= 2*blockDim values held in shared memory (in place),
@@ -148,41 +208,23 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
     a.ws_fhist[(size_t)b * E + e] = fhist[e];
   }
 
-  // ---------------- grid-wide barrier (all blocks are co-resident: cooperative launch)
-  __syncthreads();
-  if (tid == 0) {
-    int timed_out = 0;
-    __threadfence();
-    atomicAdd(a.ws_barrier, 1u);
-    const uint64_t tstart = globaltimer_ns();
-    while (true) {
-      unsigned v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.ws_barrier) : "memory");
-      if (v >= (unsigned)nblk) break;
-      if (globaltimer_ns() - tstart > a.timeout_ns) {
-        set_status(a.status, MOE_ERR_TIMEOUT);
-        timed_out = 1;
-        break;
-      }
-      __nanosleep(64);
+  // ---------------- phase B1: scan every expert column down the blocks (one warp per column)
+  if (!grid_barrier(a.ws_barrier, nblk, a.status, a.timeout_ns, &scratch[63])) return;
+  {
+    const int nwarps = blockDim.x >> 5;
+    for (int item = b * nwarps + warp; item < 2 * E; item += nblk * nwarps) {
+      int32_t* col = (item < E ? a.ws_hist : a.ws_fhist) + (item % E);
+      const int total = warp_column_scan(col, E, nblk);
+      if (lane == 0) a.ws_tot[item] = total;
     }
-    scratch[63] = timed_out;
   }
-  __syncthreads();
-  if (scratch[63] == 1) return;
+  if (!grid_barrier(a.ws_barrier + 1, nblk, a.status, a.timeout_ns, &scratch[63])) return;
 
-  // ---------------- phase B: column prefixes and expert scans
+  // ---------------- phase B2: this block's prefixes, expert scans
   for (int e = tid; e < E; e += blockDim.x) {
-    int pre = 0, tot = 0, fpre = 0, ftot = 0;
-    for (int bb = 0; bb < nblk; ++bb) {
-      const int h = __ldcg(a.ws_hist + (size_t)bb * E + e);
-      const int f = __ldcg(a.ws_fhist + (size_t)bb * E + e);
-      if (bb < b) { pre += h; fpre += f; }
-      tot += h;
-      ftot += f;
-    }
-    hist[e] = pre;      // this block's first row within expert e (relative)
-    fhist[e] = fpre;    // this block's first position within first-expert e (relative)
+    const int tot = __ldcg(a.ws_tot + e), ftot = __ldcg(a.ws_tot + E + e);
+    hist[e] = __ldcg(a.ws_hist + (size_t)b * E + e);     // this block's first row within expert e (relative)
+    fhist[e] = __ldcg(a.ws_fhist + (size_t)b * E + e);   // this block's first position within first-expert e
     eoff[e] = tot;
     toff[e] = (tot + BM - 1) / BM;
     foff[e] = ftot;
@@ -359,7 +401,7 @@ static size_t layout_smem_bytes(int E) {
 }
 
 size_t moe_layout_ws_bytes(int E) {
-  return 256 + 2 * sizeof(int32_t) * (size_t)kLayoutMaxBlocks * E;
+  return 256 + 2 * sizeof(int32_t) * (size_t)kLayoutMaxBlocks * E + 2 * sizeof(int32_t) * (size_t)E;
 }
 
 extern "C" int moe_route_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
@@ -395,6 +437,7 @@ extern "C" int moe_route_layout(const int32_t* topk_ids, const float* topk_w, co
   a.ws_barrier = reinterpret_cast<uint32_t*>(ws);
   a.ws_hist = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + 256);
   a.ws_fhist = a.ws_hist + (size_t)kLayoutMaxBlocks * L->E;
+  a.ws_tot = a.ws_fhist + (size_t)kLayoutMaxBlocks * L->E;
   a.status = status;
   a.tpb = tpb;
   a.timeout_ns = 1000000000ull;
@@ -435,7 +478,7 @@ extern "C" int moe_router_topk(const float* logits, int T, int E, int k, int32_t
 // callers that cannot allocate device memory: a plugin inside a framework
 // whose memory pool owns the whole device, a latency-critical path that must
 // not pay the device-wide synchronisation a cudaMalloc can cause, or a
-// deployment that sizes all memory once at load time.  The array (512 KiB +
+// deployment that sizes all memory once at load time.  The array (514 KiB +
 // 256 B, for up to 256 experts) is reserved on every GPU that loads the
 // library and stays there until the process exits.  The first call on a
 // device looks its address up (make that call outside any stream capture);
@@ -443,8 +486,10 @@ extern "C" int moe_router_topk(const float* logits, int T, int E, int k, int32_t
 
 namespace moe {
 constexpr int kNoAllocMaxExperts = MOE_NOALLOC_MAX_EXPERTS;
-// header (grid-barrier counter) + two per-block histograms of up to kLayoutMaxBlocks x 256 experts
-constexpr size_t kNoAllocScratchBytes = 256 + 2 * sizeof(int32_t) * (size_t)kLayoutMaxBlocks * kNoAllocMaxExperts;
+// header (grid-barrier counters) + two per-block histograms of up to kLayoutMaxBlocks x 256
+// experts + their column totals
+constexpr size_t kNoAllocScratchBytes = 256 + 2 * sizeof(int32_t) * (size_t)kLayoutMaxBlocks * kNoAllocMaxExperts +
+                                        2 * sizeof(int32_t) * (size_t)kNoAllocMaxExperts;
 }  // namespace moe
 
 static __device__ __align__(256) unsigned char g_layout_scratch[moe::kNoAllocScratchBytes];
@@ -502,12 +547,13 @@ extern "C" int moe_route_layout_noalloc(const int32_t* topk_ids, const float* to
   a.ws_barrier = reinterpret_cast<uint32_t*>(ws);
   a.ws_hist = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + 256);
   a.ws_fhist = a.ws_hist + (size_t)kLayoutMaxBlocks * L->E;
+  a.ws_tot = a.ws_fhist + (size_t)kLayoutMaxBlocks * L->E;
   a.status = status;
   a.tpb = tpb;
   a.timeout_ns = 1000000000ull;
 
-  // the array keeps the previous call's contents: the barrier counter must start at zero
-  // (the histograms are fully written before they are read)
+  // the array keeps the previous call's contents: the barrier counters must start at zero
+  // (the histograms and totals are fully written before they are read)
   if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nblk);
