@@ -182,6 +182,20 @@ MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, 
   }
 }
 
+// ---------------------------------------------------------------- cp.async (4-byte)
+
+// Asynchronous 4-byte copy global -> shared (zero-filled when src_bytes == 0,
+// in which case nothing is read).  Completion is tracked per thread by commit
+// groups.
+MOE_DEV void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+MOE_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // ---------------------------------------------------------------- TMA
 
 MOE_DEV void tma_prefetch_desc(const CUtensorMap* map) {

@@ -41,6 +41,7 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 256;
 constexpr int kGemmBK = 128;
 constexpr int kGemmStages = 4;
+constexpr int kScaleAhead = 4;   // K-blocks of block scales the promotion warps fetch ahead
 constexpr int kGemmThreads = 384;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiWarp0 = 4;                          // first promotion warp (warpgroups 1 and 2)
@@ -79,6 +80,7 @@ constexpr uint32_t kOutStageBytes = 32 * 64 * 2;
 constexpr size_t kGemmSmemBytes =
     1024 + (size_t)kGemmStages * kStageBytes + ((sizeof(GemmShared) + 127) & ~size_t(127)) +
     (size_t)kEpiWarps * kOutStageBytes;
+static_assert(kScaleAhead * 256 <= kOutStageBytes, "scale ring fits the staging tile");
 static_assert(kGemmSmemBytes <= 232448, "shared memory budget of one CTA");
 
 struct GemmParams {
@@ -277,22 +279,40 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_uni
     if (!on_unit(un.x, un.z, rows)) return;
     const int nb = un.y, e = un.z, row0 = un.w;
     const bool valid = r_in_tile < rows;
-    const float* sa_ptr = g.A_scale + row0 + r_in_tile;
+    // rows past the tile's end read nothing (zero-filled copies) from a clamped, valid address
+    const float* sa_ptr = g.A_scale + min((long long)(row0 + r_in_tile), (long long)g.R - 1);
+    const uint32_t sa_bytes = valid ? 4u : 0u;
     const float* sb_ptr = g.W_scale + ((size_t)e * nsb + (size_t)nb * 2 + h) * KB;
     float acc[128];
 #pragma unroll
     for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-    // block scales two K-blocks ahead (they come from L2)
-    float sa0 = valid ? __ldcg(sa_ptr) : 0.0f, sb0 = __ldg(sb_ptr);
-    float sa1 = (valid && KB > 1) ? __ldcg(sa_ptr + g.R) : 0.0f, sb1 = KB > 1 ? __ldg(sb_ptr + 1) : 0.0f;
-    for (int kb = 0; kb < KB; ++kb) {
-      const float sc = sa0 * sb0;
-      sa0 = sa1;
-      sb0 = sb1;
-      if (kb + 2 < KB) {
-        sa1 = valid ? __ldcg(sa_ptr + (size_t)(kb + 2) * g.R) : 0.0f;
-        sb1 = __ldg(sb_ptr + kb + 2);
+    // Block scales kScaleAhead K-blocks ahead (they come from L2): each thread
+    // keeps its own ring of (sa, sb) pairs in the warp's staging tile, filled
+    // by cp.async, so no register waits on a load in flight; one commit group
+    // per K-block (empty past the end).
+    uint8_t* stg = S.out_stage + (size_t)(warp - kEpiWarp0) * kOutStageBytes;
+    const uint32_t stg_s = smem_u32(stg);
+    const uint32_t ring = stg_s + lane * 8;           // slot i at ring + i * 256
+#pragma unroll
+    for (int i = 0; i < kScaleAhead; ++i) {
+      if (i < KB) {
+        cp_async4(ring + i * 256, sa_ptr + (size_t)i * g.R, sa_bytes);
+        cp_async4(ring + i * 256 + 4, sb_ptr + i, 4u);
       }
+      cp_async_commit();
+    }
+    for (int kb = 0; kb < KB; ++kb) {
+      const uint32_t slot = ring + (uint32_t)(kb % kScaleAhead) * 256;
+      cp_async_wait<kScaleAhead - 1>();
+      float sa, sb;
+      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(sa), "=f"(sb) : "r"(slot) : "memory");
+      const float sc = sa * sb;
+      if (kb + kScaleAhead < KB) {
+        const int kn = kb + kScaleAhead;
+        cp_async4(slot, sa_ptr + (size_t)kn * g.R, sa_bytes);
+        cp_async4(slot + 4, sb_ptr + kn, 4u);
+      }
+      cp_async_commit();
       const uint32_t p = pit & 1u, pph = (pit >> 1) & 1u;
       if (!mbar_wait(smem_u32(&sh->tfull[p]), pph, &sh->abort_flag, g.status, g.timeout_ns)) return;
       // the MMAs that read smem stage (pit % stages) are complete: hand the stage back to the TMA thread
@@ -306,9 +326,10 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_uni
       ++pit;
     }
     // bf16 output through the warp's staging tile: lane = row on the way in,
-    // 8 lanes per row (4 rows per instruction) on the way out
-    uint8_t* stg = S.out_stage + (size_t)(warp - kEpiWarp0) * kOutStageBytes;
-    const uint32_t stg_s = smem_u32(stg);
+    // 8 lanes per row (4 rows per instruction) on the way out (the scale ring
+    // there is drained: its last groups are empty)
+    cp_async_wait<0>();
+    __syncwarp();
     uint16_t* ybase = g.Y + (size_t)row0 * g.N + (size_t)nb * kGemmBN + h * 128;
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
