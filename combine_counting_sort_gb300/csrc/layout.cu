@@ -19,10 +19,12 @@
 //            tile offsets, first-expert offsets) in shared memory; block 0
 //            writes the E-sized tables, all blocks write tile tables and the
 //            rowmap grid-stride.
-//   phase C  stable ranks: warp 0 walks the block's pairs in (token, slot)
-//            order 32 at a time; lanes with equal experts find each other with
-//            __match_any_sync and take consecutive rows; warp 1 does the same
-//            for the token order by first expert.
+//   phase C  stable ranks: the block's pairs, in (token, slot) order, are cut
+//            into one contiguous slice per warp; per-warp histograms scanned
+//            across the warps give each warp its first row per expert, and each
+//            warp walks its slice 32 at a time (lanes with equal experts find
+//            each other with __match_any_sync and take consecutive rows); the
+//            token order by first expert is ranked the same way.
 //
 // Logical group g holds experts [g*E/G, (g+1)*E/G) (the Mojo EPDispatchKernel
 // page's n_local_experts = n_experts / n_ranks), so the key (group, expert)
@@ -35,6 +37,7 @@ namespace moe {
 constexpr int kLayoutThreads = 512;
 constexpr int kLayoutMaxBlocks = 256;     // bound of the workspace's per-block histograms
 constexpr int kChunkPairs = 4096;         // pairs staged in shared memory per pass
+constexpr int kLayoutWarps = kLayoutThreads / 32;
 
 struct LayoutArgs {
   const int32_t* ids;
@@ -291,7 +294,15 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
   }
   __syncthreads();
 
-  // ---------------- phase C: stable ranks within the block
+  // ---------------- phase C: stable ranks within the block, all warps
+  // Each chunk's pairs (then its tokens) are cut into one contiguous slice per
+  // warp.  A per-warp histogram of the slice, scanned across the warps on top
+  // of the block's running cursors, gives every warp its first row per
+  // expert; each warp then ranks its slice 32 at a time (lanes with equal
+  // keys find each other with __match_any_sync and take consecutive rows in
+  // lane order), which keeps the (token, slot) order stable.
+  int* whist = reinterpret_cast<int*>(s_w + kChunkPairs);   // [kLayoutWarps][E]
+  int* wh = whist + warp * E;
   for (int c0 = t0; c0 < t1; c0 += chunk_tokens) {
     const int c1 = min(t1, c0 + chunk_tokens);
     const int q0 = c0 * k, q1 = c1 * k;
@@ -303,39 +314,62 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
       }
       __syncthreads();
     }
-    if (warp == 0) {
-      for (int base = q0; base < q1; base += 32) {
-        const int p = base + lane;
-        int e = -1;
-        if (p < q1) {
-          e = s_ids[p - q0];
-          if (e < 0 || e >= E) { a.L.pair_row[p] = -1; e = -1; }
+    for (int pass = 0; pass < 2; ++pass) {
+      // pass 0: pairs [q0, q1) keyed by expert; pass 1: tokens [c0, c1) keyed by first expert
+      const int n = pass == 0 ? q1 - q0 : c1 - c0;
+      int* cursor = pass == 0 ? hist : fhist;
+      const int per = (((n + kLayoutWarps - 1) / kLayoutWarps) + 31) & ~31;
+      const int s0 = min(n, warp * per), s1 = min(n, s0 + per);
+      auto key_of = [&](int i) -> int {   // i < n; -1 for an invalid expert id
+        if (pass == 0) {
+          const int e = s_ids[i];
+          return (e < 0 || e >= E) ? -1 : e;
         }
+        const int fe = first_expert(s_ids + i * k, k, E);
+        return fe >= E ? -1 : fe;
+      };
+      for (int i = tid; i < kLayoutWarps * E; i += blockDim.x) whist[i] = 0;
+      __syncthreads();
+      for (int base = s0; base < s1; base += 32) {
+        const int i = base + lane;
+        const int e = i < s1 ? key_of(i) : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0) {
-          const int row = hist[e] + __popc(peers & lanemask_lt());
-          a.L.pair_row[p] = row;
-          a.L.row_pair[row] = p;
-          a.L.row_weight[row] = s_w[p - q0];
-        }
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) hist[e] += __popc(peers);
+        if (e >= 0 && lane == __ffs(peers) - 1) wh[e] += __popc(peers);
         __syncwarp();
       }
-    } else if (warp == 1) {
-      for (int base = c0; base < c1; base += 32) {
-        const int t = base + lane;
-        int fe = -1;
-        if (t < c1) {
-          fe = first_expert(s_ids + (t - c0) * k, k, E);
-          if (fe >= E) fe = -1;
+      __syncthreads();
+      for (int e = tid; e < E; e += blockDim.x) {
+        int run = cursor[e];
+        for (int w2 = 0; w2 < kLayoutWarps; ++w2) {
+          const int c = whist[w2 * E + e];
+          whist[w2 * E + e] = run;
+          run += c;
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, fe);
-        if (fe >= 0) a.L.token_order[fhist[fe] + __popc(peers & lanemask_lt())] = t;
+        cursor[e] = run;
+      }
+      __syncthreads();
+      for (int base = s0; base < s1; base += 32) {
+        const int i = base + lane;
+        const int e = i < s1 ? key_of(i) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int pos = e >= 0 ? wh[e] + __popc(peers & lanemask_lt()) : -1;
+        if (pass == 0) {
+          if (i < s1) {
+            const int p = q0 + i;
+            a.L.pair_row[p] = pos;
+            if (e >= 0) {
+              a.L.row_pair[pos] = p;
+              a.L.row_weight[pos] = s_w[i];
+            }
+          }
+        } else if (e >= 0) {
+          a.L.token_order[pos] = c0 + i;
+        }
         __syncwarp();
-        if (fe >= 0 && lane == __ffs(peers) - 1) fhist[fe] += __popc(peers);
+        if (e >= 0 && lane == __ffs(peers) - 1) wh[e] += __popc(peers);
         __syncwarp();
       }
+      __syncthreads();   // whist is cleared for the next pass
     }
   }
 }
@@ -397,7 +431,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 using namespace moe;
 
 static size_t layout_smem_bytes(int E) {
-  return sizeof(int) * (size_t)(2 * E + 3 * (E + 1) + 64 + kChunkPairs) + sizeof(float) * kChunkPairs;
+  return sizeof(int) * (size_t)(2 * E + 3 * (E + 1) + 64 + kChunkPairs) + sizeof(float) * kChunkPairs +
+         sizeof(int) * (size_t)kLayoutWarps * E;
 }
 
 size_t moe_layout_ws_bytes(int E) {
