@@ -520,13 +520,14 @@ def run_bw_sweep(args):
 
 
 def run_stage1_sweep(args):
-    """Fused stage1 at T=16384 Zipf(1.0): producer SMs x flag granularity x schedule vs the unfused sum."""
+    """Fused stage1 (default workload T=16384 Zipf(1.0)): producer SMs x flag granularity x schedule vs the
+    unfused sum."""
     import combine_counting_sort_gb300 as moe
     from combine_counting_sort_gb300 import inputs
     import __graft_entry__ as ge
     ge.build()
     dev = torch.device("cuda", 0)
-    cfg = inputs.CONFIGS["stage1_t16384_zipf1.0"]
+    cfg = inputs.CONFIGS[args.sweep_workload]
     wl = Workload(cfg, dev, moe.stage1_opts())
     s = torch.cuda.Stream(dev)
     moe.moe_route_layout(wl.ids, wl.w, wl.L, wl.status, stream=s)
@@ -536,7 +537,7 @@ def run_stage1_sweep(args):
                         s, args.steps, wl.flush)
     print(json.dumps({"sweep": "stage1", "workload": cfg.name, "variant": "unfused", "dispatch_us": round(disp, 1),
                       "gemm1_us": round(gemm, 1), "sum_us": round(disp + gemm, 1)}), flush=True)
-    for comm in (8, 16, 24, 36):
+    for comm in (int(c) for c in args.sweep_comm.split(",")):
         for flags in (moe.MOE_FLAGS_PER_TILE, moe.MOE_FLAGS_PER_EXPERT):
             for sched in (moe.MOE_SCHED_EXPERT_MAJOR, moe.MOE_SCHED_READY_FIRST):
                 opts = moe.stage1_opts(comm_sms=comm, flags=flags, schedule=sched, trace=1)
@@ -571,7 +572,10 @@ def main(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--sweep", choices=["bw", "stage1"], default=None,
                     help="instead of the bench line: the dispatch/combine bandwidth sweep (identity expert, "
-                         "T=2048..16384) or the fused stage1 sweep (T=16384 Zipf 1.0), one JSON line per case")
+                         "T=2048..16384) or the fused stage1 sweep, one JSON line per case")
+    ap.add_argument("--sweep-workload", default="stage1_t16384_zipf1.0",
+                    help="workload of the stage1 sweep (a name from combine_counting_sort_gb300.inputs.CONFIGS)")
+    ap.add_argument("--sweep-comm", default="8,16,24,36,48", help="producer SM counts of the stage1 sweep")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

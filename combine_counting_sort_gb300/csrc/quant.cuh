@@ -32,24 +32,31 @@ MOE_DEV void unpack16(const uint4& a, const uint4& b, float (&f)[16]) {
 // within 4 ulps of one.  In the e4m3 normal range those boundaries (midpoints
 // between adjacent codes) are exactly the fp32 values whose low 20 mantissa
 // bits are 0x80000; binade edges are codes, not boundaries.  So v' gives the
-// same code as the quotient unless its low 20 bits are within 4 of 0x80000 or
-// it lies below 2^-6 (the e4m3 subnormal range); a lane holding any such value
-// recomputes its 16 values with the IEEE division.
+// same code as the quotient unless its low 20 bits lie in a window around
+// 0x80000 or it lies below 2^-6 (the e4m3 subnormal range); a lane holding any
+// such value recomputes its 16 values with the IEEE division, and so does a
+// lane whose scale is below the fp32 normal range (where RN(1/scale) is not
+// within 2^-24, or overflows).
+//
+// The window test is ((bits(v') + 4) & 0xFFFF0) == 0x80000, i.e. low 20 bits
+// in [0x80000 - 4, 0x80000 + 11], a superset of the +-4 needed; it is folded
+// into a running minimum of ((bits + 4) & 0xFFFF0) ^ 0x80000 (zero = hit), and
+// the subnormal test into a running minimum of |v'|, so the fast path costs
+// five instructions per value.
 MOE_DEV uint4 quant16(const float (&f)[16], float scale) {
   uint32_t p[4] = {0u, 0u, 0u, 0u};
   if (scale > 0.0f) {
     const float inv = __frcp_rn(scale);
     float v[16];
-    bool slow = false;
+    uint32_t near_mid = 0xFFFFFFFFu;
+    float min_abs = INFINITY;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       v[i] = __fmul_rn(f[i], inv);
-      const uint32_t u = __float_as_uint(v[i]);
-      const uint32_t e = (u >> 23) & 0xFFu;
-      const uint32_t d = (u & 0xFFFFFu) - 0x80000u;
-      slow |= (e < 121u) | ((d + 4u) <= 8u);     // below 2^-6, or near a midpoint
+      near_mid = min(near_mid, ((__float_as_uint(v[i]) + 4u) & 0xFFFF0u) ^ 0x80000u);
+      min_abs = fminf(min_abs, fabsf(v[i]));
     }
-    if (slow) {
+    if (near_mid == 0u || min_abs < 0x1p-6f || scale < 0x1p-126f) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] = __fdiv_rn(f[i], scale);
     }

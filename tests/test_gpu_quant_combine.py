@@ -80,6 +80,23 @@ def test_weight_quant_bit_exact(E, N, H):
     assert np.array_equal(Ws.cpu().numpy().view(np.uint32), s.view(np.uint32))
 
 
+def test_weight_quant_tiny_blocks_bit_exact():
+    # blocks whose scale amax/448 is an fp32 subnormal (and bf16 subnormal weights)
+    E, N, H = 2, 256, 256
+    W = inputs.make_weights(E, N, H, seed=6).float()
+    W[0] *= 2.0 ** -118
+    W[1, :128] *= 2.0 ** -124
+    W[1, 128:] *= 2.0 ** -128
+    W = W.to(torch.bfloat16)
+    Wq = torch.empty(E, N, H, dtype=torch.uint8, device="cuda")
+    Ws = torch.empty(E, N // 128, H // 128, dtype=torch.float32, device="cuda")
+    moe.moe_quant_weights(W.cuda(), Wq, Ws)
+    torch.cuda.synchronize()
+    q, s = oracle.quantize_weights(inputs.bf16_bits(W))
+    assert np.array_equal(Wq.cpu().numpy(), q)
+    assert np.array_equal(Ws.cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
 def test_identity_expert_bit_exact():
     cfg = inputs.CONFIGS["tiny"]
     x = inputs.make_x(cfg.T, cfg.H, cfg.seed)
@@ -145,6 +162,9 @@ def test_dispatch_every_bf16_quotient_bit_exact():
     rng = np.random.default_rng(11)
     amaxes = list(oracle.bf16_to_f32(rng.integers(0x3C00, 0x4600, 24).astype(np.uint16)))
     amaxes += [1.0, 3.0, 448.0, 0.1, 7.0 / 3.0, 1e-3, 1e4]
+    # tiny blocks: scale amax/448 below the fp32 normal range (subnormal scales,
+    # bf16 subnormal inputs), where RN(1/scale) overflows or loses precision
+    amaxes += [2.0 ** -110, 2.0 ** -118, 2.0 ** -120, 2.0 ** -126, 2.0 ** -130, 2.0 ** -133]
     blocks = []
     for a in amaxes:
         ab = oracle.f64_to_bf16(np.array([a]))[0]
