@@ -60,6 +60,33 @@ def test_quant_special_blocks():
     assert q[2, 255] == (5 | 0x80)
 
 
+def test_quant_tiny_blocks_with_subnormal_scales():
+    # amax/448 below the fp32 normal range: the scale is the single rounding of
+    # the exact quotient (float64 division, then one rounding to float32, which
+    # is correct rounding for a quotient of float32 operands, subnormal results
+    # included), and every code is the e4m3 rounding of the single-rounded
+    # quotient x/scale computed the same way.  A flush-to-zero or a reciprocal
+    # shortcut fails here.
+    x = rand_bf16((4, 512), 13)
+    xv = oracle.bf16_to_f32(x).astype(np.float64)
+    xv[0] *= 2.0 ** -118
+    xv[1] *= 2.0 ** -124
+    xv[2] *= 2.0 ** -128
+    xv[3, :128] = 2.0 ** -133                  # bf16's smallest subnormal, constant block
+    xb = oracle.f64_to_bf16(xv)
+    q, s = oracle.quantize_rows(xb)
+    xf = oracle.bf16_to_f32(xb).astype(np.float64).reshape(4, 4, 128)
+    amax = np.abs(xf).max(axis=2)
+    s_ref = (amax / 448.0).astype(np.float32)
+    assert np.array_equal(s.view(np.uint32), s_ref.view(np.uint32))
+    assert np.any((s_ref > 0) & (s_ref < np.float32(2.0 ** -126)))    # the case is exercised
+    sd = s_ref.astype(np.float64)[:, :, None]
+    with np.errstate(invalid="ignore", divide="ignore"):
+        v = np.where(sd > 0, xf / sd, 0.0).astype(np.float32)
+    assert np.array_equal(q.reshape(4, 4, 128), oracle.e4m3_encode(v))
+    assert np.all(q[3, :128] == 0x7E)
+
+
 def test_dispatch_places_every_copy():
     cfg = inputs.CONFIGS["tiny"]
     x = inputs.bf16_bits(inputs.make_x(cfg.T, cfg.H))
