@@ -279,10 +279,12 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_uni
     if (!on_unit(un.x, un.z, rows)) return;
     const int nb = un.y, e = un.z, row0 = un.w;
     const bool valid = r_in_tile < rows;
-    // rows past the tile's end read nothing (zero-filled copies) from a clamped, valid address
-    const float* sa_ptr = g.A_scale + min((long long)(row0 + r_in_tile), (long long)g.R - 1);
+    // Scale addresses as 32-bit element offsets from the parameter bases (no
+    // 64-bit pointers live across the K loop).  Rows past the tile's end read
+    // nothing (zero-filled copies) from a clamped, valid address.
+    const uint32_t sa_row = (uint32_t)min((long long)(row0 + r_in_tile), (long long)g.R - 1);
     const uint32_t sa_bytes = valid ? 4u : 0u;
-    const float* sb_ptr = g.W_scale + ((size_t)e * nsb + (size_t)nb * 2 + h) * KB;
+    const uint32_t sb_off = (uint32_t)((e * nsb + nb * 2 + h) * KB);
     float acc[128];
 #pragma unroll
     for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
@@ -296,8 +298,8 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_uni
 #pragma unroll
     for (int i = 0; i < kScaleAhead; ++i) {
       if (i < KB) {
-        cp_async4(ring + i * 256, sa_ptr + (size_t)i * g.R, sa_bytes);
-        cp_async4(ring + i * 256 + 4, sb_ptr + i, 4u);
+        cp_async4(ring + i * 256, g.A_scale + (size_t)i * g.R + sa_row, sa_bytes);
+        cp_async4(ring + i * 256 + 4, g.W_scale + sb_off + i, 4u);
       }
       cp_async_commit();
     }
@@ -309,8 +311,8 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_uni
       const float sc = sa * sb;
       if (kb + kScaleAhead < KB) {
         const int kn = kb + kScaleAhead;
-        cp_async4(slot, sa_ptr + (size_t)kn * g.R, sa_bytes);
-        cp_async4(slot + 4, sb_ptr + kn, 4u);
+        cp_async4(slot, g.A_scale + (size_t)kn * g.R + sa_row, sa_bytes);
+        cp_async4(slot + 4, g.W_scale + sb_off + kn, 4u);
       }
       cp_async_commit();
       const uint32_t p = pit & 1u, pph = (pit >> 1) & 1u;
