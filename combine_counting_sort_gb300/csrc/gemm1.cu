@@ -106,6 +106,8 @@ extern "C" int moe_grouped_gemm1(const uint8_t* A, const float* A_scale, const u
   if (nsm <= 0) return MOE_ERR_CUDA;
   const long long max_units = (long long)L->max_tiles * (N / kGemmBN);
   const int grid = (int)std::max(1LL, std::min((long long)nsm, max_units));
+  static const bool split_ok = register_split_fits(grouped_gemm1_kernel);
+  if (!split_ok) return MOE_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(grouped_gemm1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;

@@ -52,6 +52,19 @@ constexpr int kEpiWarp0 = 4;                          // first promotion warp (w
 constexpr uint32_t kRegsControl = 40;
 constexpr uint32_t kRegsEpilogue = 232;
 static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= 168u * kGemmThreads, "register split exceeds launch");
+
+// setmaxnreg.inc draws on the registers the CTA was launched with (threads x
+// the kernel's per-thread count), not on the SM's register file, and waits
+// until they are free: host side, refuse the launch when the compiled kernel
+// holds fewer than the split needs, instead of launching a kernel that would
+// never get past its register re-allocation.
+template <typename Kernel>
+inline bool register_split_fits(Kernel kernel) {
+  cudaFuncAttributes a;
+  if (cudaFuncGetAttributes(&a, kernel) != cudaSuccess) return false;
+  return 128u * kRegsControl + (uint32_t)(kGemmThreads - 128) * kRegsEpilogue <=
+         (uint32_t)a.numRegs * (uint32_t)kGemmThreads;
+}
 constexpr int kUnitRing = 4;
 constexpr uint32_t kATileBytes = kGemmBM * kGemmBK;   // 16 KiB
 constexpr uint32_t kBTileBytes = kGemmBN * kGemmBK;   // 32 KiB

@@ -362,6 +362,8 @@ extern "C" int moe_stage1(const uint16_t* x, int H, const moe_layout_t* L, const
     if (!encode_u8_map(&tmA, A, 2, dA, sA, bA)) return MOE_ERR_CUDA;
     if (!encode_u8_map(&tmW, W, 3, dW, sW, bW)) return MOE_ERR_CUDA;
   }
+  static const bool split_ok = register_split_fits(stage1_kernel);
+  if (!split_ok) return MOE_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(stage1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes) !=
       cudaSuccess)
     return MOE_ERR_CUDA;

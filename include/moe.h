@@ -45,7 +45,9 @@ typedef struct CUstream_st* moe_stream_t;   /* same handle as cudaStream_t */
 typedef enum moe_status {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, workspace too small */
-  MOE_ERR_UNSUPPORTED = 2,   /* device is not sm_100-class / shape beyond a kernel limit */
+  MOE_ERR_UNSUPPORTED = 2,   /* device is not sm_100-class / shape beyond a kernel limit /
+                                the GEMM kernel's compiled register count cannot hold its
+                                warp-role register split (nothing is launched) */
   MOE_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
   MOE_ERR_EXPERT_ID = 4,     /* device: an expert id outside [0, E); the pair was skipped */
   MOE_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up (stage1 flag never set) */
