@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     regs_alloc<kRegsEpilogue>();
-    epilogue_loop(S, g, [](int, int, int) { return true; });
+    epilogue_loop(S, g);
   }
   gemm_teardown(S);
 }

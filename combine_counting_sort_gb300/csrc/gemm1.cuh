@@ -266,10 +266,9 @@ MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) 
 }
 
 // Promotion + epilogue warps (warps 4..11).  Returns when the end marker arrives.
-// `on_unit(m, e, rows)` lets the fused kernel acquire the tile's ready flag
-// before its first read of A_scale (always true for the unfused GEMM).
-template <typename OnUnit>
-MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_unit) {
+// In the fused kernel a unit reaches the ring only after the TMA warp acquired
+// its ready flag, so the A_scale reads here need no wait of their own.
+MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                 // TMEM lane quarter this warp may access
@@ -289,7 +288,6 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g, OnUnit on_uni
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&sh->uempty[slot]));
     if (un.x < 0) return;
-    if (!on_unit(un.x, un.z, rows)) return;
     const int nb = un.y, e = un.z, row0 = un.w;
     const bool valid = r_in_tile < rows;
     // Scale addresses as 32-bit element offsets from the parameter bases (no

@@ -254,8 +254,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (u == -2) { ok = false; break; }
         if (u < 0) break;
         const Unit x = unit_of(L, u, nbn);
-        ok = publish_unit(S.sh, j, x, p.g.status, p.g.timeout_ns) &&
-             wait_ready(p, x.m, x.e, x.rows, &S.sh->abort_flag, lane == 0) &&
+        // the acquire of the unit's ready flag comes before the unit is handed
+        // on: the ring's mbarrier (release here, acquire in the promotion warps)
+        // orders the producers' A_scale writes before the promotion warps' reads
+        ok = wait_ready(p, x.m, x.e, x.rows, &S.sh->abort_flag, lane == 0) &&
+             publish_unit(S.sh, j, x, p.g.status, p.g.timeout_ns) &&
              produce_unit(S, &tmA, &tmW, x, KB, it, p.g.status, p.g.timeout_ns);
         ++j;
       }
@@ -273,8 +276,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     regs_alloc<kRegsEpilogue>();
-    volatile int* ab = &S.sh->abort_flag;
-    epilogue_loop(S, p.g, [&](int m, int e, int rows) { return wait_ready(p, m, e, rows, ab); });
+    epilogue_loop(S, p.g);
   }
   gemm_teardown(S);
   if (p.trace && threadIdx.x == 0) atomicMax(p.tr + MOE_TRACE_END, (unsigned long long)globaltimer_ns());
