@@ -555,6 +555,31 @@ def run_bw_sweep(args):
         del x, A, As, Y, out, L
 
 
+def run_layout_sweep(args):
+    """Routing layout call latency vs batch (E=256, k=8, Zipf 1.2 routing): one
+    block in a plain launch up to T = 32, the cooperative grid above."""
+    import combine_counting_sort_gb300 as moe
+    from combine_counting_sort_gb300 import inputs
+    import __graft_entry__ as ge
+    ge.build()
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    E, G, k = 256, 8, 8
+    for T in (8, 32, 33, 128, 512, 2048, 8192, 16384):
+        logits = inputs.make_logits(T, E, 1.2, 0).to(dev)
+        ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+        w = torch.empty(T, k, dtype=torch.float32, device=dev)
+        moe.moe_router_topk(logits, k, ids, w)
+        L = moe.Layout(T, k, E, G, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        us = _time_events(lambda: moe.moe_route_layout(ids, w, L, st, stream=s), s, args.steps, flush)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        print(json.dumps({"sweep": "layout", "T": T, "k": k, "E": E, "pairs": T * k, "layout_us": round(us, 1),
+                          "blocks": "one (plain launch)" if T <= 32 else "grid (cooperative)"}), flush=True)
+
+
 def run_stage1_sweep(args):
     """Fused stage1 (default workload T=16384 Zipf(1.0)): producer SMs x flag granularity x schedule vs the
     unfused sum."""
@@ -606,9 +631,9 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--sweep", choices=["bw", "stage1"], default=None,
+    ap.add_argument("--sweep", choices=["bw", "stage1", "layout"], default=None,
                     help="instead of the bench line: the dispatch/combine bandwidth sweep (identity expert, "
-                         "T=2048..16384) or the fused stage1 sweep, one JSON line per case")
+                         "T=2048..16384), the fused stage1 sweep or the layout latency sweep, one JSON line per case")
     ap.add_argument("--sweep-workload", default="stage1_t16384_zipf1.0",
                     help="workload of the stage1 sweep (a name from combine_counting_sort_gb300.inputs.CONFIGS)")
     ap.add_argument("--sweep-comm", default="8,16,24,36,48", help="producer SM counts of the stage1 sweep")
@@ -621,6 +646,8 @@ def main(argv=None):
         run_bw_sweep(args)
     elif args.sweep == "stage1":
         run_stage1_sweep(args)
+    elif args.sweep == "layout":
+        run_layout_sweep(args)
     else:
         run_gpu(args)
 

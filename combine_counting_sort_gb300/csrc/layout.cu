@@ -206,31 +206,44 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
     }
     __syncthreads();
   }
-  for (int e = tid; e < E; e += blockDim.x) {
-    a.ws_hist[(size_t)b * E + e] = hist[e];
-    a.ws_fhist[(size_t)b * E + e] = fhist[e];
-  }
-
-  // ---------------- phase B1: scan every expert column down the blocks (one warp per column)
-  if (!grid_barrier(a.ws_barrier, nblk, a.status, a.timeout_ns, &scratch[63])) return;
-  {
-    const int nwarps = blockDim.x >> 5;
-    for (int item = b * nwarps + warp; item < 2 * E; item += nblk * nwarps) {
-      int32_t* col = (item < E ? a.ws_hist : a.ws_fhist) + (item % E);
-      const int total = warp_column_scan(col, E, nblk);
-      if (lane == 0) a.ws_tot[item] = total;
+  if (nblk == 1) {
+    // one block (small batches, a plain launch): its histograms are the totals
+    // and its prefixes are zero; no workspace, no grid barrier
+    for (int e = tid; e < E; e += blockDim.x) {
+      const int tot = hist[e], ftot = fhist[e];
+      hist[e] = 0;
+      fhist[e] = 0;
+      eoff[e] = tot;
+      toff[e] = (tot + BM - 1) / BM;
+      foff[e] = ftot;
     }
-  }
-  if (!grid_barrier(a.ws_barrier + 1, nblk, a.status, a.timeout_ns, &scratch[63])) return;
+  } else {
+    for (int e = tid; e < E; e += blockDim.x) {
+      a.ws_hist[(size_t)b * E + e] = hist[e];
+      a.ws_fhist[(size_t)b * E + e] = fhist[e];
+    }
 
-  // ---------------- phase B2: this block's prefixes, expert scans
-  for (int e = tid; e < E; e += blockDim.x) {
-    const int tot = __ldcg(a.ws_tot + e), ftot = __ldcg(a.ws_tot + E + e);
-    hist[e] = __ldcg(a.ws_hist + (size_t)b * E + e);     // this block's first row within expert e (relative)
-    fhist[e] = __ldcg(a.ws_fhist + (size_t)b * E + e);   // this block's first position within first-expert e
-    eoff[e] = tot;
-    toff[e] = (tot + BM - 1) / BM;
-    foff[e] = ftot;
+    // ---------------- phase B1: scan every expert column down the blocks (one warp per column)
+    if (!grid_barrier(a.ws_barrier, nblk, a.status, a.timeout_ns, &scratch[63])) return;
+    {
+      const int nwarps = blockDim.x >> 5;
+      for (int item = b * nwarps + warp; item < 2 * E; item += nblk * nwarps) {
+        int32_t* col = (item < E ? a.ws_hist : a.ws_fhist) + (item % E);
+        const int total = warp_column_scan(col, E, nblk);
+        if (lane == 0) a.ws_tot[item] = total;
+      }
+    }
+    if (!grid_barrier(a.ws_barrier + 1, nblk, a.status, a.timeout_ns, &scratch[63])) return;
+
+    // ---------------- phase B2: this block's prefixes, expert scans
+    for (int e = tid; e < E; e += blockDim.x) {
+      const int tot = __ldcg(a.ws_tot + e), ftot = __ldcg(a.ws_tot + E + e);
+      hist[e] = __ldcg(a.ws_hist + (size_t)b * E + e);     // this block's first row within expert e (relative)
+      fhist[e] = __ldcg(a.ws_fhist + (size_t)b * E + e);   // this block's first position within first-expert e
+      eoff[e] = tot;
+      toff[e] = (tot + BM - 1) / BM;
+      foff[e] = ftot;
+    }
   }
   __syncthreads();
   const int total_rows = block_exclusive_scan(eoff, E, scratch);
@@ -255,11 +268,14 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
     for (int g = tid; g <= a.L.G; g += blockDim.x) a.L.group_offset[g] = eoff[g * epg];
     if (tid == 0) a.L.num_tiles[0] = total_tiles;
   }
-  // tile tables and rowmap, grid-stride over all blocks
+  // tile tables and rowmap: one warp per tile, grid-stride over all blocks'
+  // warps; one search for the tile's expert, then the tile's BM rowmap slots
+  // in coalesced runs of 32 (per-slot searches cost ~1 us more per call)
   {
-    const int gtid = b * blockDim.x + tid, gstride = nblk * blockDim.x;
+    const int nwarps = blockDim.x >> 5;
+    const int gw = b * nwarps + warp, gwstride = nblk * nwarps;
     const int cap = a.L.max_tiles;
-    for (int m = gtid; m < cap; m += gstride) {
+    for (int m = gw; m < cap; m += gwstride) {
       int e = -1, begin = T * k, rows = 0;
       if (m < total_tiles) {
         int lo = 0, hi = E;                 // largest e with toff[e] <= m
@@ -268,28 +284,16 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
           if (toff[mid] <= m) lo = mid; else hi = mid;
         }
         e = lo;
-        const int i = m - toff[e];
-        begin = eoff[e] + i * BM;
+        begin = eoff[e] + (m - toff[e]) * BM;
         rows = min(BM, eoff[e + 1] - begin);
       }
-      a.L.tile_expert[m] = e;
-      a.L.tile_row_begin[m] = begin;
-      a.L.tile_rows[m] = rows;
-    }
-    const long long slots = (long long)cap * BM;
-    for (long long s = gtid; s < slots; s += gstride) {
-      const int m = (int)(s / BM), j = (int)(s % BM);
-      int v = -1;
-      if (m < total_tiles) {
-        int lo = 0, hi = E;
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (toff[mid] <= m) lo = mid; else hi = mid;
-        }
-        const int begin = eoff[lo] + (m - toff[lo]) * BM;
-        if (begin + j < eoff[lo + 1]) v = begin + j;
+      if (lane == 0) {
+        a.L.tile_expert[m] = e;
+        a.L.tile_row_begin[m] = begin;
+        a.L.tile_rows[m] = rows;
       }
-      a.L.rowmap[s] = v;
+      int32_t* slot = a.L.rowmap + (size_t)m * BM;
+      for (int j = lane; j < BM; j += 32) slot[j] = j < rows ? begin + j : -1;
     }
   }
   __syncthreads();
@@ -439,14 +443,10 @@ size_t moe_layout_ws_bytes(int E) {
   return 256 + 2 * sizeof(int32_t) * (size_t)kLayoutMaxBlocks * E + 2 * sizeof(int32_t) * (size_t)E;
 }
 
-extern "C" int moe_route_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
-                                void* ws, size_t ws_bytes, int32_t* status, moe_stream_t stream) {
-  int rc = check_layout(L);
-  if (rc) return rc;
-  if (!topk_ids || !topk_w || !ws) return MOE_ERR_INVALID_ARG;
-  if (ws_bytes < moe_layout_ws_bytes(L->E)) return MOE_ERR_INVALID_ARG;
-  if (((uintptr_t)ws & 15) != 0) return MOE_ERR_INVALID_ARG;
-  cudaStream_t s = (cudaStream_t)stream;
+// Grid, workspace pointers and launch shared by both entry points.  `ws` is
+// the caller's workspace or the library's fixed scratch.
+static int launch_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L, void* ws,
+                         int32_t* status, cudaStream_t s) {
   int dev, nsm;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -458,12 +458,17 @@ extern "C" int moe_route_layout(const int32_t* topk_ids, const float* topk_w, co
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_layout_kernel, kLayoutThreads, smem) != cudaSuccess || per_sm < 1)
     return MOE_ERR_CUDA;
-  // one block per SM at most, at least ~32 tokens per block
+  // One block per SM at most, ~32 tokens per block.  The tile tables and the
+  // rowmap (max_tiles x 128 slots, most of them -1 on small batches) are
+  // written one tile per warp over the whole grid, and one SM writes them
+  // slowly, so a grid of more than one block has at least one warp per tile
+  // (blocks past the last token have empty ranges).  A single block (T <= 32)
+  // runs as a plain launch with no workspace memset and no grid barrier.
   int nblk = (L->T + 31) / 32;
+  if (nblk > 1) nblk = std::max(nblk, (L->max_tiles + kLayoutWarps - 1) / kLayoutWarps);
   nblk = std::min(nblk, std::min(nsm * per_sm, std::min(nsm, kLayoutMaxBlocks)));
   nblk = std::max(nblk, 1);
   const int tpb = (L->T + nblk - 1) / nblk;
-  nblk = (L->T + tpb - 1) / tpb;
 
   LayoutArgs a;
   a.ids = topk_ids;
@@ -477,6 +482,13 @@ extern "C" int moe_route_layout(const int32_t* topk_ids, const float* topk_w, co
   a.tpb = tpb;
   a.timeout_ns = 1000000000ull;
 
+  if (nblk == 1) {
+    route_layout_kernel<<<1, kLayoutThreads, smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  // the grid barriers' counters start at zero (the workspace, or the fixed
+  // scratch, keeps whatever the previous call left; the histograms and totals
+  // are fully written before they are read)
   if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nblk);
@@ -490,6 +502,16 @@ extern "C" int moe_route_layout(const int32_t* topk_ids, const float* topk_w, co
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, route_layout_kernel, a) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+extern "C" int moe_route_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
+                                void* ws, size_t ws_bytes, int32_t* status, moe_stream_t stream) {
+  int rc = check_layout(L);
+  if (rc) return rc;
+  if (!topk_ids || !topk_w || !ws) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_layout_ws_bytes(L->E)) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)ws & 15) != 0) return MOE_ERR_INVALID_ARG;
+  return launch_layout(topk_ids, topk_w, L, ws, status, (cudaStream_t)stream);
 }
 
 extern "C" int moe_router_topk(const float* logits, int T, int E, int k, int32_t* topk_ids,
@@ -558,48 +580,5 @@ extern "C" int moe_route_layout_noalloc(const int32_t* topk_ids, const float* to
   void* ws = nullptr;
   rc = layout_scratch_address(&ws);
   if (rc) return rc;
-  cudaStream_t s = (cudaStream_t)stream;
-  int dev, nsm;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
-
-  const size_t smem = layout_smem_bytes(L->E);
-  if (cudaFuncSetAttribute(route_layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_layout_kernel, kLayoutThreads, smem) != cudaSuccess || per_sm < 1)
-    return MOE_ERR_CUDA;
-  int nblk = (L->T + 31) / 32;
-  nblk = std::min(nblk, std::min(nsm * per_sm, std::min(nsm, kLayoutMaxBlocks)));
-  nblk = std::max(nblk, 1);
-  const int tpb = (L->T + nblk - 1) / nblk;
-  nblk = (L->T + tpb - 1) / tpb;
-
-  LayoutArgs a;
-  a.ids = topk_ids;
-  a.w = topk_w;
-  a.L = to_dev(L);
-  a.ws_barrier = reinterpret_cast<uint32_t*>(ws);
-  a.ws_hist = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + 256);
-  a.ws_fhist = a.ws_hist + (size_t)kLayoutMaxBlocks * L->E;
-  a.ws_tot = a.ws_fhist + (size_t)kLayoutMaxBlocks * L->E;
-  a.status = status;
-  a.tpb = tpb;
-  a.timeout_ns = 1000000000ull;
-
-  // the array keeps the previous call's contents: the barrier counters must start at zero
-  // (the histograms and totals are fully written before they are read)
-  if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nblk);
-  cfg.blockDim = dim3(kLayoutThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, route_layout_kernel, a) != cudaSuccess) return MOE_ERR_CUDA;
-  return MOE_OK;
+  return launch_layout(topk_ids, topk_w, L, ws, status, (cudaStream_t)stream);
 }

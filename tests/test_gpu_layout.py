@@ -30,6 +30,8 @@ def test_layout_matches_oracle_on_workloads(name):
     (1, 1, 1, 1, "uniform"), (3, 2, 4, 2, "uniform"), (37, 4, 16, 4, "dup"), (500, 6, 64, 8, "one_expert"),
     (1000, 32, 1024, 4, "uniform"), (129, 8, 256, 8, "skew"), (100000, 8, 256, 8, "skew"),
     (70000, 1, 3, 1, "uniform"),
+    # either side of the single-block (plain launch) limit of 32 tokens
+    (32, 8, 256, 8, "skew"), (33, 8, 256, 8, "skew"), (32, 32, 64, 4, "uniform"),
 ])
 def test_layout_edge_cases(T, k, E, G, mode):
     rng = np.random.default_rng(T + k + E)
