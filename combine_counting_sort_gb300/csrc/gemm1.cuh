@@ -8,23 +8,25 @@
 // of one expert times 256 output columns, the full K = H.
 //
 // Per CTA (one per SM, 384 threads = 3 warpgroups):
-//   warp 0, lane 0   claims units, publishes them through a shared-memory ring,
-//                    and streams the K-blocks (128 FP8 values of K) of A
-//                    (2-D TMA, rows [row0, row0+128) of the dense buffer, the
-//                    rowmap's first slot of the tile) and of W (3-D TMA, rows
-//                    [nb*256, +256) of expert e) into a 4-stage ring, 128-byte
-//                    swizzled.
-//   warp 1, lane 0   issues 4 tcgen05.mma (K=32 each, M=128, N=256, e4m3 x e4m3
-//                    -> fp32) per K-block into one of two TMEM partial buffers
-//                    (2 x 256 columns), committing to the smem-stage barrier
-//                    and the partial-ready barrier.
+//   warp 0           (converged; one elected lane issues) claims units,
+//                    publishes them through a shared-memory ring, and streams
+//                    the K-blocks (128 FP8 values of K) of A (2-D TMA, rows
+//                    [row0, row0+128) of the dense buffer, the rowmap's first
+//                    slot of the tile) and of W (3-D TMA, rows [nb*256, +256)
+//                    of expert e) into a 4-stage ring, 128-byte swizzled.
+//   warp 1           (converged; one elected lane issues) 4 tcgen05.mma (K=32
+//                    each, M=128, N=256, e4m3 x e4m3 -> fp32) per K-block into
+//                    one of two TMEM partial buffers (2 x 256 columns) and one
+//                    commit to that buffer's partial-ready barrier; the
+//                    promotion warps hand the smem stage back when they see it.
 //   warps 2, 3       idle (they complete warpgroup 0, whose registers go to
 //                    the promotion warpgroups: setmaxnreg 40 / 232).
 //   warps 4..11      promotion: each thread owns one row (TMEM lane) and 128
 //                    columns; per K-block it loads the fp32 partial and folds it
 //                    into register accumulators with the two block scales,
-//                    acc += partial * (sa[row, kb] * sb[e, n/128, kb]); after the
-//                    last K-block it rounds to bf16 and stores the valid rows.
+//                    acc += partial * (sa[row, kb] * sb[e, n/128, kb]), the two
+//                    scales fetched ahead by cp.async; after the last K-block it
+//                    rounds to bf16 and stores the valid rows.
 //
 // fp32 block scales per 128 values are not a tensor-core mode (the hardware
 // block-scaled kinds take power-of-two scales per 32), so the scales are
