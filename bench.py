@@ -140,8 +140,9 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
 # ---------------------------------------------------------------- the GPU arm
@@ -280,7 +281,10 @@ def run_gpu(args):
     e2e = run_e2e(wl, s, args, world, device)
 
     peaks = measured_peaks()
-    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    # the roofline kernel runs inside a ~1 s loop of steps (power-capped clocks):
+    # the sustained measured peak is its denominator; the burst one is reported beside it
+    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    fp8_burst = peaks["bf16_tflops"] * FP8_OVER_BF16
     stage_avg = statistics.mean(stage_ms) if fused else u_gemm
     variant_key = "%s/comm%d/%s/%s/join%d" % (args.variant, args.comm_sms, ["per_tile", "per_expert"][args.flags],
                                               ["expert_major", "ready_first"][args.schedule], args.join)
@@ -302,7 +306,9 @@ def run_gpu(args):
         "roofline": {"kernel": "stage1_kernel" if fused else "grouped_gemm1_kernel", "bound": "tensor",
                      "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / fp8_peak, 4),
-                     "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (fp8/bf16 nominal)",
+                     "peak_source": f"{peaks['source']} bf16 sustained x {FP8_OVER_BF16} (fp8/bf16 nominal); "
+                                    "the kernel is timed inside a long loop of steps",
+                     "peak_burst": round(fp8_burst, 1), "frac_of_burst": round(achieved / fp8_burst, 4),
                      "traffic": traffic,
                      "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one full-size launch"
                      if traffic is not None else None},
@@ -623,7 +629,7 @@ def run_stage1_sweep(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)   # ~1 s timed: several clock samples under load
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="t8192_zipf1.2")
