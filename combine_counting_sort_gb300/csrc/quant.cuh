@@ -27,44 +27,56 @@ MOE_DEV void unpack16(const uint4& a, const uint4& b, float (&f)[16]) {
 // -> codes 0.
 //
 // Fast path: v' = RN(x * RN(1/scale)).  Both roundings are relative errors of
-// at most 2^-24, so v' is within 3 fp32 ulps of the exact quotient RN(x/scale),
-// and both lie on the same side of every e4m3 rounding boundary unless v' is
-// within 4 ulps of one.  In the e4m3 normal range those boundaries (midpoints
-// between adjacent codes) are exactly the fp32 values whose low 20 mantissa
-// bits are 0x80000; binade edges are codes, not boundaries.  So v' gives the
-// same code as the quotient unless its low 20 bits lie in a window around
-// 0x80000 or it lies below 2^-6 (the e4m3 subnormal range); a lane holding any
-// such value recomputes its 16 values with the IEEE division, and so does a
-// lane whose scale is below the fp32 normal range (where RN(1/scale) is not
-// within 2^-24, or overflows).
+// at most 2^-24, so v' is within 3 * 2^-24 (relative) of the exact quotient
+// q = RN(x/scale).  The e4m3 rounding (nearest-even, saturating) is monotonic,
+// so if it maps the bracket lo = RN(v' * (1 - 2^-21)) and hi = RN(v' *
+// (1 + 2^-21)) to the same code, q (inside the bracket: 2^-21 - 2^-24 >
+// 3 * 2^-24) has that code too.  Where v' is an fp32 subnormal the bounds do
+// not hold, but there |q| < 2^-10 as well and both round to the signed zero of
+// their (exact) sign.
 //
-// The window test is ((bits(v') + 4) & 0xFFFF0) == 0x80000, i.e. low 20 bits
-// in [0x80000 - 4, 0x80000 + 11], a superset of the +-4 needed; it is folded
-// into a running minimum of ((bits + 4) & 0xFFFF0) ^ 0x80000 (zero = hit), and
-// the subnormal test into a running minimum of |v'|, so the fast path costs
-// five instructions per value.
+// A value whose bracket straddles a rounding boundary takes the IEEE division,
+// and so does every value of a lane whose scale is below the fp32 normal range
+// (RN(1/scale) not within 2^-24, or overflowing).  With bf16 inputs straddling
+// is common (q often lands exactly on a midpoint between two codes: ~0.5% of
+// values, so most warps hold one somewhere in a 16-value round), so only the
+// flagged values are divided: the warp loops while any lane has one left,
+// each lane taking its next flagged value (selected from the 16 by compare
+// and select, so nothing is indexed dynamically).  Whole warp, converged.
 MOE_DEV uint4 quant16(const float (&f)[16], float scale) {
+  constexpr float kBelow = 1.0f - 0x1p-21f, kAbove = 1.0f + 0x1p-21f;
   uint32_t p[4] = {0u, 0u, 0u, 0u};
+  uint32_t need = 0u;   // bit j: value j takes the IEEE division
   if (scale > 0.0f) {
     const float inv = __frcp_rn(scale);
-    float v[16];
-    uint32_t near_mid = 0xFFFFFFFFu;
-    float min_abs = INFINITY;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      v[i] = __fmul_rn(f[i], inv);
-      near_mid = min(near_mid, ((__float_as_uint(v[i]) + 4u) & 0xFFFF0u) ^ 0x80000u);
-      min_abs = fminf(min_abs, fabsf(v[i]));
-    }
-    if (near_mid == 0u || min_abs < 0x1p-6f || scale < 0x1p-126f) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = __fdiv_rn(f[i], scale);
-    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = e4m3x2(v[4 * i + 0], v[4 * i + 1]);
-      const uint32_t hi = e4m3x2(v[4 * i + 2], v[4 * i + 3]);
-      p[i] = lo | (hi << 16);
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = __fmul_rn(f[4 * i + j], inv);
+      const uint32_t below = e4m3x2(__fmul_rn(v[0], kBelow), __fmul_rn(v[1], kBelow)) |
+                             ((uint32_t)e4m3x2(__fmul_rn(v[2], kBelow), __fmul_rn(v[3], kBelow)) << 16);
+      const uint32_t above = e4m3x2(__fmul_rn(v[0], kAbove), __fmul_rn(v[1], kAbove)) |
+                             ((uint32_t)e4m3x2(__fmul_rn(v[2], kAbove), __fmul_rn(v[3], kAbove)) << 16);
+      // one bit per differing byte: bytes 0..3 -> bits 0..3 (the multiply gathers them into bits 24..27)
+      const uint32_t bytes = __vcmpne4(below, above) & 0x01010101u;
+      need |= ((bytes * 0x01020408u) >> 24) << (4 * i);
+      p[i] = below;
+    }
+    if (scale < 0x1p-126f) need = 0xFFFFu;
+  }
+  while (__any_sync(0xffffffffu, need != 0u)) {
+    if (need != 0u) {
+      const int j = __ffs(need) - 1;
+      need &= need - 1u;
+      float xj = f[0];
+#pragma unroll
+      for (int k = 1; k < 16; ++k) xj = j == k ? f[k] : xj;
+      const uint32_t c = e4m3x2(__fdiv_rn(xj, scale), 0.0f) & 0xFFu;
+      const int w = j >> 2, sh = (j & 3) * 8;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (w == k) p[k] = (p[k] & ~(0xFFu << sh)) | (c << sh);
     }
   }
   return make_uint4(p[0], p[1], p[2], p[3]);
