@@ -217,6 +217,21 @@ MOE_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int
       : "memory");
 }
 
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA / bulk copy) reads of them.
+MOE_DEV void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Bulk copy shared -> global (this thread's bulk async-group); the source must
+// be visible to the async proxy first (fence.proxy.async.shared::cta).
+MOE_DEV void bulk_copy_to_global(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               :: "l"(reinterpret_cast<uint64_t>(dst)), "r"(src), "r"(bytes) : "memory");
+}
+MOE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// all but this thread's newest N bulk groups are complete (their writes performed)
+template <int N>
+MOE_DEV void bulk_wait() { asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory"); }
+
 // ---------------------------------------------------------------- tcgen05 / TMEM
 
 MOE_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

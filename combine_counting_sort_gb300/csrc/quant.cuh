@@ -138,6 +138,49 @@ MOE_DEV void quant_scatter_slice(const uint16_t* __restrict__ x, int H, int t, i
   }
 }
 
+// As quant_scatter_slice, but the codes go to shared memory (the row's bytes
+// [c0, c0 + 512*ROUNDS) at row_s + c0, 16 bytes per lane per round) for bulk
+// copies to the token's rows; the block scales still go to every row directly.
+template <int ROUNDS>
+MOE_DEV void quant_stage_slice(const uint16_t* __restrict__ x, int H, int t, int c0, int k, long long R,
+                               int myrow, float* __restrict__ A_scale, uint32_t row_s) {
+  const int lane = threadIdx.x & 31;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  uint4 raw[2 * ROUNDS];
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    const int col = c0 + r * 512 + lane * 16;
+    raw[2 * r] = make_uint4(0, 0, 0, 0);
+    raw[2 * r + 1] = raw[2 * r];
+    if (col < H) {
+      raw[2 * r] = __ldcs(xr + col / 8);
+      raw[2 * r + 1] = __ldcs(xr + col / 8 + 1);
+    }
+  }
+  float sc[ROUNDS];
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    float f[16];
+    unpack16(raw[2 * r], raw[2 * r + 1], f);
+    sc[r] = __fdiv_rn(block_amax8(f), 448.0f);
+    const uint4 q = quant16(f, sc[r]);
+    const int col = c0 + r * 512 + lane * 16;
+    if (col < H)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_s + (uint32_t)col), "r"(q.x), "r"(q.y),
+                   "r"(q.z), "r"(q.w)
+                   : "memory");
+  }
+  for (int j = 0; j < k; ++j) {
+    const int row = __shfl_sync(0xffffffffu, myrow, j);
+    if (row < 0) continue;
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+      const int col = c0 + r * 512 + lane * 16;
+      if (col < H && (lane & 7) == 0) A_scale[(size_t)(col / kQBlock) * R + row] = sc[r];
+    }
+  }
+}
+
 // Quantise token t once (scale = amax/448 per 128 values) and store codes and
 // scales to each of its k rows; `myrow` is pair_row[t*k + lane] for lanes < k
 // (-1 elsewhere / for skipped pairs).  Whole warp, converged.

@@ -83,30 +83,81 @@ MOE_DEV bool wait_ready(const Stage1Params& p, int m, int e, int rows, volatile 
   return true;
 }
 
-// Producer warp: tokens token_order[i] for i = gw, gw + PW, ...
+// Lane j < k publishes its row of the token (per-tile or per-expert flag),
+// after a fence that orders the row's writes before the release.
+MOE_DEV void publish_row(const Stage1Params& p, int row, const int* s_eoff, const int* s_toff) {
+  if (row < 0) return;
+  int lo = 0, hi = p.g.L.E;                     // expert of the row: largest e with eoff[e] <= row
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_eoff[mid] <= row) lo = mid; else hi = mid;
+  }
+  const int m = s_toff[lo] + (row - s_eoff[lo]) / kGemmBM;
+  if (m != p.withhold_tile) {
+    __threadfence();
+    red_release_gpu_add(p.per_expert ? p.expert_flag + lo : p.tile_flag + m, 1);
+  }
+}
+
+// Producer warp: tokens token_order[i] for i = gw, gw + PW, ..., each
+// quantised once in 2048-column chunks (4 KB of the row in flight) and stored
+// to its k rows with 16-byte stores, then published.
 MOE_DEV void produce_tokens(const Stage1Params& p, int gw, int PW, const int* s_eoff, const int* s_toff) {
   const int lane = threadIdx.x & 31;
   const LayoutDev& L = p.g.L;
-  const int T = L.T, k = L.k, E = L.E;
+  const int T = L.T, k = L.k;
   for (int i = gw; i < T; i += PW) {
     const int t = L.token_order[i];
     const int myrow = lane < k ? L.pair_row[(size_t)t * k + lane] : -1;
-    for (int c0 = 0; c0 < p.g.H; c0 += 2048)     // 2048-column chunks: 4 KB of the row in flight
+    for (int c0 = 0; c0 < p.g.H; c0 += 2048)
       quant_scatter_slice<4>(p.x, p.g.H, t, c0, k, p.g.R, myrow, p.A, p.A_scale);
     fence_proxy_async_global();
     __syncwarp();
-    if (myrow >= 0) {
-      int lo = 0, hi = E;                       // expert of the row: largest e with eoff[e] <= row
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_eoff[mid] <= myrow) lo = mid; else hi = mid;
-      }
-      const int m = s_toff[lo] + (myrow - s_eoff[lo]) / kGemmBM;
-      if (m != p.withhold_tile) {
-        __threadfence();
-        red_release_gpu_add(p.per_expert ? p.expert_flag + lo : p.tile_flag + m, 1);
-      }
+    publish_row(p, myrow, s_eoff, s_toff);
+  }
+}
+
+// The same with the code rows written by bulk copies (the TMA engine, not the
+// warp's 16-byte stores, which set a producer SM's pace): the token's codes
+// are staged in one of two row buffers of `stg` (2 x H bytes), and lane j < k
+// copies the row to A row j.  A token is published one token later, once its
+// copies are complete (wait_group 1), so the copies of token i overlap the
+// quantisation of token i+1; that wait also frees the buffer token i+2 reuses.
+MOE_DEV void produce_tokens_bulk(const Stage1Params& p, int gw, int PW, const int* s_eoff, const int* s_toff,
+                                 uint32_t stg) {
+  const int lane = threadIdx.x & 31;
+  const LayoutDev& L = p.g.L;
+  const int T = L.T, k = L.k, H = p.g.H;
+  int prev_row = -1;
+  bool have_prev = false;
+  uint32_t buf = 0;
+  for (int i = gw; i < T; i += PW) {
+    const int t = L.token_order[i];
+    const int myrow = lane < k ? L.pair_row[(size_t)t * k + lane] : -1;
+    const uint32_t row_s = stg + buf * (uint32_t)H;
+    for (int c0 = 0; c0 < H; c0 += 2048)
+      quant_stage_slice<4>(p.x, H, t, c0, k, p.g.R, myrow, p.A_scale, row_s);
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane < k) {
+      if (myrow >= 0) bulk_copy_to_global(p.A + (size_t)myrow * H, row_s, (uint32_t)H);
+      bulk_commit();
     }
+    if (have_prev) {
+      if (lane < k) bulk_wait<1>();            // the previous token's copies are complete
+      fence_proxy_async_global();
+      __syncwarp();
+      publish_row(p, prev_row, s_eoff, s_toff);
+    }
+    prev_row = myrow;
+    have_prev = true;
+    buf ^= 1u;
+  }
+  if (have_prev) {
+    if (lane < k) bulk_wait<0>();
+    fence_proxy_async_global();
+    __syncwarp();
+    publish_row(p, prev_row, s_eoff, s_toff);
   }
 }
 
@@ -224,7 +275,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int gw = blockIdx.x * nw + warp;
       int PW = p.S * nw;
       if (p.ready_first) { PW -= 1; if (gw > nw - 1) gw -= 1; }
-      produce_tokens(p, gw, PW, s_eoff, s_toff);
+      // two staging rows per warp after the offset tables and the scheduler's
+      // bitmap, when they fit in the idle stage buffers
+      const size_t bitmap_bytes = ((size_t)L.max_tiles + 31) / 32 * 4;
+      const size_t table_end =
+          ((size_t)(reinterpret_cast<uint8_t*>(s_done) - S.stages) + bitmap_bytes + 1023) & ~size_t(1023);
+      if (table_end + (size_t)nw * 2 * p.g.H <= (size_t)kGemmStages * kStageBytes)
+        produce_tokens_bulk(p, gw, PW, s_eoff, s_toff,
+                            smem_u32(S.stages + table_end + (size_t)warp * 2 * p.g.H));
+      else
+        produce_tokens(p, gw, PW, s_eoff, s_toff);
     }
     // the stage buffers go back to the TMA (async proxy) after generic-proxy use
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -102,6 +102,16 @@ def test_stage1_comm_sm_counts(small, comm):
     small.check_same_as_unfused(moe.stage1_opts(comm_sms=comm))
 
 
+def test_stage1_wide_rows():
+    # H = 8192: two staging rows per producer warp no longer fit in the idle
+    # stage buffers, so the producers store code rows directly instead of by
+    # bulk copies; the result is the same
+    cfg = inputs.MoEConfig("wide", T=300, H=8192, E=8, G=2, k=4, N=256, zipf=1.2, seed=9)
+    P = Problem(cfg)
+    for opts in (moe.stage1_opts(comm_sms=8), moe.stage1_opts(comm_sms=24, schedule=moe.MOE_SCHED_READY_FIRST)):
+        P.check_same_as_unfused(opts)
+
+
 @pytest.mark.parametrize("name", ["t8192_zipf1.2"])
 def test_stage1_full_size_bit_identical_to_unfused(name):
     P = Problem(inputs.CONFIGS[name])
