@@ -1,0 +1,68 @@
+"""The whole step (routing layout, fused stage1, combine) captured into one CUDA
+graph and replayed gives the same bytes as the eager calls: the calls do no
+host synchronisation and keep every count on the device."""
+import numpy as np
+import pytest
+import torch
+
+import combine_counting_sort_gb300 as moe
+from combine_counting_sort_gb300 import inputs
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    gu.build()
+
+
+def test_step_replays_from_a_cuda_graph():
+    cfg = inputs.MoEConfig("graph", T=600, H=512, E=32, G=4, k=4, N=512, zipf=1.2, seed=12)
+    ids, w = gu.routed(cfg)
+    dev = "cuda"
+    x = inputs.make_x(cfg.T, cfg.H, cfg.seed).to(dev)
+    ids_d, w_d = torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev)
+    W = inputs.make_weights(cfg.E, cfg.N, cfg.H, cfg.seed, device=dev)
+    Wq = torch.empty(cfg.E, cfg.N, cfg.H, dtype=torch.uint8, device=dev)
+    Ws = torch.empty(cfg.E, cfg.N // 128, cfg.H // 128, dtype=torch.float32, device=dev)
+    moe.moe_quant_weights(W, Wq, Ws)
+    R = cfg.T * cfg.k
+    L = moe.Layout(cfg.T, cfg.k, cfg.E, cfg.G, device=dev)
+    A = torch.empty(R, cfg.H, dtype=torch.uint8, device=dev)
+    As = torch.empty(cfg.H // 128, R, dtype=torch.float32, device=dev)
+    Y = torch.empty(R, cfg.N, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(cfg.T, cfg.N, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(int(L.sizes.stage1_ws_bytes), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    opts = moe.stage1_opts(comm_sms=8)
+
+    def step():
+        moe.moe_route_layout(ids_d, w_d, L, status)
+        moe.moe_stage1(x, L, Wq, Ws, A, As, Y, ws, status, opts)
+        moe.moe_combine(Y, L, out, status)
+
+    step()
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    want_out, want_y = out.clone(), Y.clone()
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()                                   # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for t in (out, Y):
+        t.fill_(float("nan"))
+    for t in L.t.values():
+        t.fill_(-7)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(out.view(torch.int16), want_out.view(torch.int16))
+    assert torch.equal(Y.view(torch.int16), want_y.view(torch.int16))
