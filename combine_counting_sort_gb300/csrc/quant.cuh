@@ -97,7 +97,8 @@ MOE_DEV float block_amax8(const float (&f)[16]) {
 // token's hidden dimension shared by several warps): all 2*ROUNDS 16-byte
 // loads of the lane are issued before any arithmetic, so each warp keeps
 // ROUNDS KB of the row in flight; then the 512-column rounds are quantised
-// and stored to the token's k rows.  `myrow` as in quant_scatter_token.
+// and stored to the token's k rows.  `myrow` is pair_row[t*k + lane] for
+// lanes < k (-1 elsewhere / for skipped pairs).  Whole warp, converged.
 template <int ROUNDS>
 MOE_DEV void quant_scatter_slice(const uint16_t* __restrict__ x, int H, int t, int c0, int k, long long R,
                                  int myrow, uint8_t* __restrict__ A, float* __restrict__ A_scale) {
@@ -177,43 +178,6 @@ MOE_DEV void quant_stage_slice(const uint16_t* __restrict__ x, int H, int t, int
     for (int r = 0; r < ROUNDS; ++r) {
       const int col = c0 + r * 512 + lane * 16;
       if (col < H && (lane & 7) == 0) A_scale[(size_t)(col / kQBlock) * R + row] = sc[r];
-    }
-  }
-}
-
-// Quantise token t once (scale = amax/448 per 128 values) and store codes and
-// scales to each of its k rows; `myrow` is pair_row[t*k + lane] for lanes < k
-// (-1 elsewhere / for skipped pairs).  Whole warp, converged.
-MOE_DEV void quant_scatter_token(const uint16_t* __restrict__ x, int H, int t, int k, long long R, int myrow,
-                                 uint8_t* __restrict__ A, float* __restrict__ A_scale) {
-  const int lane = threadIdx.x & 31;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-  for (int c0 = 0; c0 < H; c0 += 1024) {
-    // two rounds of 512 values in flight
-    const int colA = c0 + lane * 16, colB = colA + 512;
-    const bool actA = colA < H, actB = colB < H;
-    uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, b0 = a0, b1 = a0;
-    if (actA) { a0 = __ldcs(xr + colA / 8); a1 = __ldcs(xr + colA / 8 + 1); }
-    if (actB) { b0 = __ldcs(xr + colB / 8); b1 = __ldcs(xr + colB / 8 + 1); }
-    float fa[16], fb[16];
-    unpack16(a0, a1, fa);
-    unpack16(b0, b1, fb);
-    const float sA = __fdiv_rn(block_amax8(fa), 448.0f);
-    const float sB = __fdiv_rn(block_amax8(fb), 448.0f);
-    const uint4 qA = quant16(fa, sA);
-    const uint4 qB = quant16(fb, sB);
-    for (int j = 0; j < k; ++j) {
-      const int r = __shfl_sync(0xffffffffu, myrow, j);
-      if (r < 0) continue;
-      uint8_t* arow = A + (size_t)r * H;
-      if (actA) {
-        *reinterpret_cast<uint4*>(arow + colA) = qA;
-        if ((lane & 7) == 0) A_scale[(size_t)(colA / kQBlock) * R + r] = sA;
-      }
-      if (actB) {
-        *reinterpret_cast<uint4*>(arow + colB) = qB;
-        if ((lane & 7) == 0) A_scale[(size_t)(colB / kQBlock) * R + r] = sB;
-      }
     }
   }
 }
