@@ -97,6 +97,11 @@ MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// A packed pair of fp32 values (low half first) -> two bf16 values.
+MOE_DEV uint32_t pack_bf16x2_from_pair(unsigned long long v) {
+  return pack_bf16x2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
+}
+
 // Two fp32 -> two e4m3 codes (round to nearest even, saturate to +-448); lo in the low byte.
 MOE_DEV uint16_t e4m3x2(float lo, float hi) {
   return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);

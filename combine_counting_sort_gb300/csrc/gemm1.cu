@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     regs_alloc<kRegsEpilogue>();
-    epilogue_loop(S, g);
+    epilogue_loop<true>(S, g);
   }
   gemm_teardown(S);
 }

@@ -267,9 +267,38 @@ MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) 
   }
 }
 
+// The promotion warps' accumulators, one row x 128 columns per thread: plain
+// fp32 values folded with fma.rn.f32, or packed pairs folded with
+// fma.rn.f32x2 (bit-identical sums).
+template <bool kPacked>
+struct FoldAcc;
+
+template <>
+struct FoldAcc<false> {
+  float v[128];
+  MOE_DEV void zero() {
+#pragma unroll
+    for (int i = 0; i < 128; ++i) v[i] = 0.0f;
+  }
+  MOE_DEV void fold(uint32_t taddr, float sc) { tmem_fold128(taddr, sc, v); }
+  MOE_DEV uint32_t bf16x2(int c) const { return pack_bf16x2(v[c], v[c + 1]); }   // columns c, c + 1
+};
+
+template <>
+struct FoldAcc<true> {
+  unsigned long long v[64];   // column 2i in the low half, 2i + 1 in the high half
+  MOE_DEV void zero() {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = 0ull;
+  }
+  MOE_DEV void fold(uint32_t taddr, float sc) { tmem_fold128x2(taddr, sc, v); }
+  MOE_DEV uint32_t bf16x2(int c) const { return pack_bf16x2_from_pair(v[c / 2]); }   // c even
+};
+
 // Promotion + epilogue warps (warps 4..11).  Returns when the end marker arrives.
 // In the fused kernel a unit reaches the ring only after the TMA warp acquired
 // its ready flag, so the A_scale reads here need no wait of their own.
+template <bool kPacked>
 MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -298,9 +327,8 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
     const uint32_t sa_row = (uint32_t)min((long long)(row0 + r_in_tile), (long long)g.R - 1);
     const uint32_t sa_bytes = valid ? 4u : 0u;
     const uint32_t sb_off = (uint32_t)((e * nsb + nb * 2 + h) * KB);
-    float acc[128];
-#pragma unroll
-    for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+    FoldAcc<kPacked> acc;
+    acc.zero();
     // Block scales kScaleAhead K-blocks ahead (they come from L2): each thread
     // keeps its own ring of (sa, sb) pairs in the warp's staging tile, filled
     // by cp.async, so no register waits on a load in flight; one commit group
@@ -334,7 +362,7 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
       if (warp == kEpiWarp0 && lane == 0) mbar_arrive(smem_u32(&sh->empty[pit % kGemmStages]));
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + p * kGemmBN + h * 128;
-      tmem_fold128(taddr, sc, acc);
+      acc.fold(taddr, sc);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[p]));
@@ -353,8 +381,8 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
         const int a = pass * 64 + c * 8;
         const uint32_t dst = stg_s + lane * 128 + ((c ^ (lane & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                     "r"(pack_bf16x2(acc[a + 0], acc[a + 1])), "r"(pack_bf16x2(acc[a + 2], acc[a + 3])),
-                     "r"(pack_bf16x2(acc[a + 4], acc[a + 5])), "r"(pack_bf16x2(acc[a + 6], acc[a + 7]))
+                     "r"(acc.bf16x2(a + 0)), "r"(acc.bf16x2(a + 2)), "r"(acc.bf16x2(a + 4)),
+                     "r"(acc.bf16x2(a + 6))
                      : "memory");
       }
       __syncwarp();

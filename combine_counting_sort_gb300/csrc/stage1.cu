@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     regs_alloc<kRegsEpilogue>();
-    epilogue_loop(S, p.g);
+    epilogue_loop<false>(S, p.g);
   }
   gemm_teardown(S);
   if (p.trace && threadIdx.x == 0) atomicMax(p.tr + MOE_TRACE_END, (unsigned long long)globaltimer_ns());

@@ -1,15 +1,21 @@
 // tmem_fold.cuh: acc[0..127] += sc * (128 consecutive fp32 TMEM columns of
-// this thread's lane), as ONE inline-asm statement.
+// this thread's lane), as ONE inline-asm statement, in two forms.
 //
 // Four 32-column tcgen05.ld loads; each load after the first is issued before
-// the previous chunk's 32 FMAs, so the TMEM read latency overlaps arithmetic,
+// the previous chunk's FMAs, so the TMEM read latency overlaps arithmetic,
 // and the temporaries live only inside the statement (the compiler cannot
-// stretch their lifetimes across chunks, which is what pushed the register
-// count past the budget of a 320-thread CTA).  The 128 accumulators are
-// in/out operands; `taddr` is the TMEM address of column 0 (lane field set by
-// the caller), `sc` the per-row block-scale product.
-// The statement below is spelled out in full: four loads into two banks of
-// 32 registers (t0-31, t32-63), then fma.rn.f32 acc_i = t_i * sc + acc_i.
+// stretch their lifetimes across chunks).  `taddr` is the TMEM address of
+// column 0 (lane field set by the caller), `sc` the per-row block-scale
+// product.  The statements are spelled out in full: four loads into two banks
+// of 32 registers (t0-31, t32-63), then the FMAs.
+//
+// tmem_fold128 keeps 128 fp32 accumulators and folds with fma.rn.f32.
+// tmem_fold128x2 keeps them as 64 packed pairs (column 2i in the low half of
+// acc[i], 2i+1 in the high half) and folds with the packed fma.rn.f32x2: two
+// independent fp32 FMAs, each rounded like fma.rn.f32, so the sums are
+// bit-for-bit the same with half the FMA instructions.  Which one is faster
+// depends on the kernel around it (the standalone GEMM1: the packed form by
+// 4%; the fused stage1 kernel: the scalar form by 3%, measured on one box).
 #pragma once
 
 #include "common.cuh"
@@ -76,6 +82,46 @@ MOE_DEV void tmem_fold128(uint32_t taddr, float sc, float (&acc)[128]) {
         "+f"(acc[104]), "+f"(acc[105]), "+f"(acc[106]), "+f"(acc[107]), "+f"(acc[108]), "+f"(acc[109]), "+f"(acc[110]), "+f"(acc[111]),
         "+f"(acc[112]), "+f"(acc[113]), "+f"(acc[114]), "+f"(acc[115]), "+f"(acc[116]), "+f"(acc[117]), "+f"(acc[118]), "+f"(acc[119]),
         "+f"(acc[120]), "+f"(acc[121]), "+f"(acc[122]), "+f"(acc[123]), "+f"(acc[124]), "+f"(acc[125]), "+f"(acc[126]), "+f"(acc[127])
+      : "r"(taddr), "f"(sc)
+      : "memory");
+}
+
+MOE_DEV void tmem_fold128x2(uint32_t taddr, float sc, unsigned long long (&acc)[64]) {
+  asm volatile(
+      "{\n\t.reg .b32 t<64>;\n\t.reg .b64 s2, pt;\n\tmov.b64 s2, {%65, %65};\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%64+0];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t32, t33, t34, t35, t36, t37, t38, t39, t40, t41, t42, t43, t44, t45, t46, t47, t48, t49, t50, t51, t52, t53, t54, t55, t56, t57, t58, t59, t60, t61, t62, t63}, [%64+32];\n\t"
+      "mov.b64 pt, {t0, t1}; fma.rn.f32x2 %0, pt, s2, %0; mov.b64 pt, {t2, t3}; fma.rn.f32x2 %1, pt, s2, %1; mov.b64 pt, {t4, t5}; fma.rn.f32x2 %2, pt, s2, %2; mov.b64 pt, {t6, t7}; fma.rn.f32x2 %3, pt, s2, %3;\n\t"
+      "mov.b64 pt, {t8, t9}; fma.rn.f32x2 %4, pt, s2, %4; mov.b64 pt, {t10, t11}; fma.rn.f32x2 %5, pt, s2, %5; mov.b64 pt, {t12, t13}; fma.rn.f32x2 %6, pt, s2, %6; mov.b64 pt, {t14, t15}; fma.rn.f32x2 %7, pt, s2, %7;\n\t"
+      "mov.b64 pt, {t16, t17}; fma.rn.f32x2 %8, pt, s2, %8; mov.b64 pt, {t18, t19}; fma.rn.f32x2 %9, pt, s2, %9; mov.b64 pt, {t20, t21}; fma.rn.f32x2 %10, pt, s2, %10; mov.b64 pt, {t22, t23}; fma.rn.f32x2 %11, pt, s2, %11;\n\t"
+      "mov.b64 pt, {t24, t25}; fma.rn.f32x2 %12, pt, s2, %12; mov.b64 pt, {t26, t27}; fma.rn.f32x2 %13, pt, s2, %13; mov.b64 pt, {t28, t29}; fma.rn.f32x2 %14, pt, s2, %14; mov.b64 pt, {t30, t31}; fma.rn.f32x2 %15, pt, s2, %15;\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%64+64];\n\t"
+      "mov.b64 pt, {t32, t33}; fma.rn.f32x2 %16, pt, s2, %16; mov.b64 pt, {t34, t35}; fma.rn.f32x2 %17, pt, s2, %17; mov.b64 pt, {t36, t37}; fma.rn.f32x2 %18, pt, s2, %18; mov.b64 pt, {t38, t39}; fma.rn.f32x2 %19, pt, s2, %19;\n\t"
+      "mov.b64 pt, {t40, t41}; fma.rn.f32x2 %20, pt, s2, %20; mov.b64 pt, {t42, t43}; fma.rn.f32x2 %21, pt, s2, %21; mov.b64 pt, {t44, t45}; fma.rn.f32x2 %22, pt, s2, %22; mov.b64 pt, {t46, t47}; fma.rn.f32x2 %23, pt, s2, %23;\n\t"
+      "mov.b64 pt, {t48, t49}; fma.rn.f32x2 %24, pt, s2, %24; mov.b64 pt, {t50, t51}; fma.rn.f32x2 %25, pt, s2, %25; mov.b64 pt, {t52, t53}; fma.rn.f32x2 %26, pt, s2, %26; mov.b64 pt, {t54, t55}; fma.rn.f32x2 %27, pt, s2, %27;\n\t"
+      "mov.b64 pt, {t56, t57}; fma.rn.f32x2 %28, pt, s2, %28; mov.b64 pt, {t58, t59}; fma.rn.f32x2 %29, pt, s2, %29; mov.b64 pt, {t60, t61}; fma.rn.f32x2 %30, pt, s2, %30; mov.b64 pt, {t62, t63}; fma.rn.f32x2 %31, pt, s2, %31;\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t32, t33, t34, t35, t36, t37, t38, t39, t40, t41, t42, t43, t44, t45, t46, t47, t48, t49, t50, t51, t52, t53, t54, t55, t56, t57, t58, t59, t60, t61, t62, t63}, [%64+96];\n\t"
+      "mov.b64 pt, {t0, t1}; fma.rn.f32x2 %32, pt, s2, %32; mov.b64 pt, {t2, t3}; fma.rn.f32x2 %33, pt, s2, %33; mov.b64 pt, {t4, t5}; fma.rn.f32x2 %34, pt, s2, %34; mov.b64 pt, {t6, t7}; fma.rn.f32x2 %35, pt, s2, %35;\n\t"
+      "mov.b64 pt, {t8, t9}; fma.rn.f32x2 %36, pt, s2, %36; mov.b64 pt, {t10, t11}; fma.rn.f32x2 %37, pt, s2, %37; mov.b64 pt, {t12, t13}; fma.rn.f32x2 %38, pt, s2, %38; mov.b64 pt, {t14, t15}; fma.rn.f32x2 %39, pt, s2, %39;\n\t"
+      "mov.b64 pt, {t16, t17}; fma.rn.f32x2 %40, pt, s2, %40; mov.b64 pt, {t18, t19}; fma.rn.f32x2 %41, pt, s2, %41; mov.b64 pt, {t20, t21}; fma.rn.f32x2 %42, pt, s2, %42; mov.b64 pt, {t22, t23}; fma.rn.f32x2 %43, pt, s2, %43;\n\t"
+      "mov.b64 pt, {t24, t25}; fma.rn.f32x2 %44, pt, s2, %44; mov.b64 pt, {t26, t27}; fma.rn.f32x2 %45, pt, s2, %45; mov.b64 pt, {t28, t29}; fma.rn.f32x2 %46, pt, s2, %46; mov.b64 pt, {t30, t31}; fma.rn.f32x2 %47, pt, s2, %47;\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "mov.b64 pt, {t32, t33}; fma.rn.f32x2 %48, pt, s2, %48; mov.b64 pt, {t34, t35}; fma.rn.f32x2 %49, pt, s2, %49; mov.b64 pt, {t36, t37}; fma.rn.f32x2 %50, pt, s2, %50; mov.b64 pt, {t38, t39}; fma.rn.f32x2 %51, pt, s2, %51;\n\t"
+      "mov.b64 pt, {t40, t41}; fma.rn.f32x2 %52, pt, s2, %52; mov.b64 pt, {t42, t43}; fma.rn.f32x2 %53, pt, s2, %53; mov.b64 pt, {t44, t45}; fma.rn.f32x2 %54, pt, s2, %54; mov.b64 pt, {t46, t47}; fma.rn.f32x2 %55, pt, s2, %55;\n\t"
+      "mov.b64 pt, {t48, t49}; fma.rn.f32x2 %56, pt, s2, %56; mov.b64 pt, {t50, t51}; fma.rn.f32x2 %57, pt, s2, %57; mov.b64 pt, {t52, t53}; fma.rn.f32x2 %58, pt, s2, %58; mov.b64 pt, {t54, t55}; fma.rn.f32x2 %59, pt, s2, %59;\n\t"
+      "mov.b64 pt, {t56, t57}; fma.rn.f32x2 %60, pt, s2, %60; mov.b64 pt, {t58, t59}; fma.rn.f32x2 %61, pt, s2, %61; mov.b64 pt, {t60, t61}; fma.rn.f32x2 %62, pt, s2, %62; mov.b64 pt, {t62, t63}; fma.rn.f32x2 %63, pt, s2, %63;\n\t"
+      "}"
+      : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]),
+        "+l"(acc[8]), "+l"(acc[9]), "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]), "+l"(acc[14]), "+l"(acc[15]),
+        "+l"(acc[16]), "+l"(acc[17]), "+l"(acc[18]), "+l"(acc[19]), "+l"(acc[20]), "+l"(acc[21]), "+l"(acc[22]), "+l"(acc[23]),
+        "+l"(acc[24]), "+l"(acc[25]), "+l"(acc[26]), "+l"(acc[27]), "+l"(acc[28]), "+l"(acc[29]), "+l"(acc[30]), "+l"(acc[31]),
+        "+l"(acc[32]), "+l"(acc[33]), "+l"(acc[34]), "+l"(acc[35]), "+l"(acc[36]), "+l"(acc[37]), "+l"(acc[38]), "+l"(acc[39]),
+        "+l"(acc[40]), "+l"(acc[41]), "+l"(acc[42]), "+l"(acc[43]), "+l"(acc[44]), "+l"(acc[45]), "+l"(acc[46]), "+l"(acc[47]),
+        "+l"(acc[48]), "+l"(acc[49]), "+l"(acc[50]), "+l"(acc[51]), "+l"(acc[52]), "+l"(acc[53]), "+l"(acc[54]), "+l"(acc[55]),
+        "+l"(acc[56]), "+l"(acc[57]), "+l"(acc[58]), "+l"(acc[59]), "+l"(acc[60]), "+l"(acc[61]), "+l"(acc[62]), "+l"(acc[63])
       : "r"(taddr), "f"(sc)
       : "memory");
 }
