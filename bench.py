@@ -413,14 +413,23 @@ def run_e2e(wl, s, args, world, device):
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
 
 class CpuSample:
-    """The oracle, as it stands, on a bounded sample of the workload.
+    """The oracle, as it stands, on a bounded sample of the workload, scaled to
+    a whole step of T tokens.
 
     Untimed set-up: inputs, the router's top-k pairs (input preparation, not a
-    step of the path) and the sample experts' weights as random finite e4m3
-    codes with fp32 block scales (weights are quantised offline; the oracle's
-    time does not depend on their values).  Timed: the routing layout of all T
-    tokens, then quant + dispatch + GEMM1 + combine over the rows of the first
-    non-empty experts in expert-major order until the budget is spent."""
+    step of the path), one layout and one quantisation of every token (to hand
+    GEMM1 its operands), random bf16 expert outputs for the combine sample,
+    and one expert's weights as random finite e4m3 codes
+    with fp32 block scales, used for every sampled expert (weights are
+    quantised offline and the oracle's time does not depend on their values).  Timed pieces:
+      * fixed(): the routing layout of all T tokens (whole), then quant +
+        dispatch and combine of a seeded sample of tokens (each x T / sample);
+      * expert(): GEMM1 over all rows of one non-empty expert, the experts
+        taken in a seeded random order without repetition (cycling once all
+        are done); the mean over the experts timed, x the number of non-empty
+        experts, estimates the whole GEMM1 call (exact once every expert has
+        been timed)."""
+    TOKENS = 64
 
     def __init__(self, cfg):
         import numpy as np
@@ -430,80 +439,117 @@ class CpuSample:
         self.x = inputs.bf16_bits(inputs.make_x(cfg.T, cfg.H, cfg.seed))
         logits = inputs.make_logits(cfg.T, cfg.E, cfg.zipf, cfg.seed).numpy()
         self.ids, self.w = oracle.router_topk(logits, cfg.k)
+        self.L = oracle.route_layout(self.ids, self.w, cfg.E, cfg.G)
+        self.q, self.sc = oracle.quantize_rows(self.x)
+        eo = self.L["expert_offset"]
         self.rng = np.random.default_rng(cfg.seed)
-        self.weights = {}
+        self.order = self.rng.permutation(np.nonzero(eo[1:] > eo[:-1])[0])
+        self.tokens = min(self.TOKENS, cfg.T)
+        self.t_fixed, self.t_experts = [], []
+        self.codes = self.rng.integers(0, 0x7E, size=(1, cfg.N, cfg.H), dtype=np.uint8)
+        self.codes |= self.rng.integers(0, 2, size=self.codes.shape, dtype=np.uint8) << 7
+        self.scales = np.full((1, cfg.N // 128, cfg.H // 128), 1.0 / (448.0 * math.sqrt(cfg.H)), np.float32)
+        self.Y = oracle.f64_to_bf16(self.rng.standard_normal((self.tokens * cfg.k, cfg.N)))   # GEMM1 rows to combine
 
-    def expert_weights(self, e):
-        np, cfg = self.np, self.cfg
-        if e not in self.weights:
-            codes = self.rng.integers(0, 0x7E, size=(1, cfg.N, cfg.H), dtype=np.uint8)
-            codes |= (self.rng.integers(0, 2, size=codes.shape, dtype=np.uint8) << 7)
-            scales = np.full((1, cfg.N // 128, cfg.H // 128), 1.0 / (448.0 * math.sqrt(cfg.H)), np.float32)
-            self.weights[e] = (codes, scales)
-        return self.weights[e]
-
-    def run(self, budget_s: float):
+    def fixed(self) -> float:
         np, oracle, cfg = self.np, self.oracle, self.cfg
-        timed = 0.0
+        S = self.tokens
         t0 = time.perf_counter()
-        L = oracle.route_layout(self.ids, self.w, cfg.E, cfg.G)
-        timed += time.perf_counter() - t0
+        oracle.route_layout(self.ids, self.w, cfg.E, cfg.G)
+        t_layout = time.perf_counter() - t0
+
+        toks = self.rng.choice(cfg.T, S, replace=False)
+        t0 = time.perf_counter()
+        q, sc = oracle.quantize_rows(self.x[toks])
+        oracle.dispatch(q, sc, np.arange(S * cfg.k), cfg.k)
+        t_quant = time.perf_counter() - t0
+
+        toks = self.rng.choice(cfg.T, S, replace=False)
+        t0 = time.perf_counter()
+        oracle.combine(self.Y, np.arange(S * cfg.k), self.w[toks])
+        t_comb = time.perf_counter() - t0
+        self.t_fixed.append(t_layout + (t_quant + t_comb) * cfg.T / S)
+        return t_layout + t_quant + t_comb
+
+    def expert(self) -> float:
+        np, oracle, cfg, L = self.np, self.oracle, self.cfg, self.L
+        e = int(self.order[len(self.t_experts) % len(self.order)])
         eo = L["expert_offset"]
-        rows_done, experts_done = 0, 0
-        for e in range(cfg.E):
-            if eo[e + 1] == eo[e]:
-                continue
-            Wq, Ws = self.expert_weights(e)
-            t0 = time.perf_counter()
-            rows = np.arange(eo[e], eo[e + 1])
-            pairs = L["row_pair"][rows]
-            toks, inv = np.unique(pairs // cfg.k, return_inverse=True)
-            q, sc = oracle.quantize_rows(self.x[toks])
-            A, As = q[inv], np.ascontiguousarray(sc[inv].T)         # dispatch of the sample rows
-            Yb = oracle.grouped_gemm1(A, As, Wq, Ws, np.array([0, len(rows)]))
-            # combine work of these rows: each row weighted into its token's accumulator
-            oracle.combine(Yb, np.arange(len(rows)), np.asarray(L["row_weight"][rows], np.float32)[:, None])
-            timed += time.perf_counter() - t0
-            rows_done += len(rows)
-            experts_done += 1
-            if timed > budget_s:
-                break
-        tok_per_s = (rows_done / cfg.k) / timed
-        desc = (f"timed: layout of all {cfg.T} tokens + quant/dispatch/GEMM1/combine over the rows of the first "
-                f"{experts_done} non-empty experts ({rows_done} of {cfg.T * cfg.k} rows); value = rows/k per second")
-        return tok_per_s, desc, timed
+        toks = L["row_pair"][eo[e]:eo[e + 1]] // cfg.k
+        A, As = self.q[toks], np.ascontiguousarray(self.sc[toks].T)
+        t0 = time.perf_counter()
+        oracle.grouped_gemm1(A, As, self.codes, self.scales, np.array([0, len(toks)]))
+        t = time.perf_counter() - t0
+        self.t_experts.append(t)
+        return t
+
+    def step_ms(self) -> float:
+        """Estimated oracle time of one whole step, from every piece timed so far."""
+        return 1e3 * (statistics.mean(self.t_fixed) + statistics.mean(self.t_experts) * len(self.order))
+
+    def describe(self) -> str:
+        cfg = self.cfg
+        return (f"{len(self.t_fixed)} x (layout of all {cfg.T} tokens; quant+dispatch and combine of "
+                f"{self.tokens} sampled tokens) and GEMM1 of {len(self.t_experts)} sampled experts (all their rows, "
+                f"of {len(self.order)} non-empty); each piece scaled to a whole step, value = T / that time")
 
 
 def cpu_baseline(cfg, budget_s):
-    v, desc, el = CpuSample(cfg).run(budget_s)
-    return {"value": round(v, 2), "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": desc, "seconds": round(el, 2)}
+    sample = CpuSample(cfg)
+    timed = sample.fixed()
+    while not sample.t_experts or timed < budget_s:
+        timed += sample.expert()
+    return {"value": round(cfg.T / (sample.step_ms() / 1e3), 2), "unit": UNIT, "cores": cpu_threads(),
+            "kind": "oracle", "sample": sample.describe(), "seconds": round(timed, 2)}
+
+
+def cpu_threads() -> int:
+    """Threads the oracle's numpy kernels may use: the BLAS pool if one is
+    reported, else the cores this process may run on."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p["num_threads"] for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except ImportError:
+        pass
+    return len(os.sched_getaffinity(0))
 
 
 def run_reference(args):
-    """Reference arm of this tier: the CPU oracle timed on the host cores."""
+    """Reference arm of this tier: the CPU oracle timed on the host cores.  Each
+    step times the fixed pieces of a sampled step (CpuSample.fixed, ~0.1 s)
+    and then experts' GEMM1 while the step's share of --ref-budget-s (with
+    what earlier steps left unspent) lasts, so that a run takes about that
+    budget plus 0.1 s per step."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     from combine_counting_sort_gb300 import inputs
     cfg = inputs.CONFIGS[args.workload]
-    per_step = max(2.0, args.cpu_budget_s / max(1, args.steps))
     sample = CpuSample(cfg)
-    sample.run(0.5)                      # warm-up: one expert
-    vals, descs, secs = [], [], 0.0
+    for _ in range(args.warmup):         # untimed warm-up of the fixed pieces
+        sample.fixed()
+    sample.t_fixed.clear()
+    share, bank, secs = args.ref_budget_s / max(1, args.steps), 0.0, 0.0
     for _ in range(args.steps):
-        v, d, el = sample.run(per_step)
-        vals.append(v)
-        descs.append(d)
-        secs += el
-    value = statistics.mean(vals)
+        bank += share
+        secs += sample.fixed()
+        while bank > 0:
+            t = sample.expert()
+            bank -= t
+            secs += t
+    if not sample.t_experts:
+        secs += sample.expert()
+    ms_per_step = sample.step_ms()
+    value = cfg.T / (ms_per_step / 1e3)
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 1),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 quant)",
             "data": "synthetic (seeded)", "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E,
                                                       "G": cfg.G, "k": cfg.k, "N": cfg.N, "zipf": cfg.zipf},
-            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
-                             "kind": "oracle", "sample": descs[-1]},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": sample.describe(), "seconds_timed": round(secs, 2)},
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -640,7 +686,9 @@ def main(argv=None):
     ap.add_argument("--join", type=int, default=1, help="producer CTAs take GEMM work when done")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the roofline kernel from an ncu capture (else null)")
-    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="seconds of oracle work of the cpu_baseline")
+    ap.add_argument("--ref-budget-s", type=float, default=40.0,
+                    help="seconds of sampled oracle GEMM1 in a whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--sweep", choices=["bw", "stage1", "layout"], default=None,

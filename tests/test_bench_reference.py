@@ -1,0 +1,58 @@
+"""The benchmark's reference arm (the CPU oracle on the host cores): its JSON
+line, its sampler's coverage of the experts, and that ranks other than 0 do
+no work.  CPU only."""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+from combine_counting_sort_gb300 import inputs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(extra_env=None, *args):
+    env = dict(os.environ, **(extra_env or {}))
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", *args],
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return r.stdout
+
+
+def test_reference_line_tiny_workload():
+    out = _run(None, "--workload", "tiny", "--steps", "3", "--warmup", "3", "--ref-budget-s", "2")
+    lines = [l for l in out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["steps"] == 3 and line["warmup"] == 3 and line["config"]["workload"] == "tiny"
+    assert line["value"] > 0
+    # ms_per_step is the estimated time of one whole step of T tokens
+    T = inputs.CONFIGS["tiny"].T
+    assert abs(T / (line["ms_per_step"] / 1e3) - line["value"]) <= 0.01 * line["value"] + 0.01
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    out = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, "--workload", "tiny", "--steps", "3",
+               "--warmup", "3", "--ref-budget-s", "2")
+    assert not [l for l in out.splitlines() if l.startswith("{")]
+
+
+def test_sampler_times_every_nonempty_expert_once_before_repeating():
+    cfg = inputs.CONFIGS["tiny"]
+    s = bench.CpuSample(cfg)
+    eo = s.L["expert_offset"]
+    nonempty = {e for e in range(cfg.E) if eo[e + 1] > eo[e]}
+    assert set(int(e) for e in s.order) == nonempty and len(s.order) == len(nonempty)
+    for _ in range(len(s.order)):
+        s.expert()
+    s.fixed()
+    assert len(s.t_experts) == len(nonempty)
+    # with every expert timed once, the GEMM1 part of the estimate is their sum
+    gemm_ms = s.step_ms() - 1e3 * s.t_fixed[0]
+    assert abs(gemm_ms - 1e3 * sum(s.t_experts)) <= 1e-6 * gemm_ms
