@@ -108,7 +108,7 @@ def sample_rows(r, n_experts=10, seed=0):
     return np.unique(np.array(rows, dtype=np.int64))
 
 
-@pytest.mark.parametrize("name", ["t2048_uniform", "t8192_zipf1.2"])
+@pytest.mark.parametrize("name", ["t2048_uniform", "t8192_zipf1.2", "stage1_t16384_zipf1.0"])
 def test_gemm1_full_size_sampled(name):
     cfg = inputs.CONFIGS[name]
     W = inputs.make_weights(cfg.E, cfg.N, cfg.H, cfg.seed, device="cuda")

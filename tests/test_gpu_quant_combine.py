@@ -195,3 +195,37 @@ def test_dispatch_every_bf16_quotient_bit_exact():
     A_ref, As_ref = oracle.dispatch(q, s, L["pair_row"].cpu().numpy(), k)
     assert np.array_equal(A.cpu().numpy(), A_ref)
     assert np.array_equal(As.cpu().numpy().view(np.uint32), As_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("name", ["bw_t4096", "bw_t8192", "bw_t16384", "stage1_t16384_zipf1.0"])
+def test_dispatch_identity_combine_full_size_sampled(name):
+    # The bandwidth sweep's sizes and the T=16384 workload, run in full on the
+    # device as the benchmark launches them, checked on sampled tokens (the
+    # first, the last and 254 random ones): their k rows of codes, scales and
+    # identity-expert outputs bit-exact, their combined output within the
+    # tolerance, and the dequantised-input invariant.
+    cfg = inputs.CONFIGS[name]
+    x = inputs.make_x(cfg.T, cfg.H, cfg.seed)
+    ids, w, L, A, As = dispatch_on_gpu(cfg, x)
+    R, k = cfg.T * cfg.k, cfg.k
+    Y = torch.empty(R, cfg.H, dtype=torch.bfloat16, device="cuda")
+    moe.moe_dequant_rows(A, As, L, Y)
+    out = torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_combine(Y, L, out, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    rng = np.random.default_rng(cfg.T)
+    toks = np.unique(np.concatenate([[0, cfg.T - 1], rng.choice(cfg.T, 254, replace=False)]))
+    S = len(toks)
+    rows = torch.from_numpy(L["pair_row"].cpu().numpy().reshape(cfg.T, k)[toks].reshape(-1).astype(np.int64)).cuda()
+    q, s = oracle.quantize_rows(inputs.bf16_bits(x)[toks])
+    A_s, As_s = A.index_select(0, rows).cpu().numpy(), As.index_select(1, rows).cpu().numpy()
+    assert np.array_equal(A_s, np.repeat(q, k, axis=0))                       # row t*k + j holds token t
+    assert np.array_equal(As_s.view(np.uint32), np.repeat(s.T, k, axis=1).view(np.uint32))
+    Y_ref = oracle.identity_expert(A_s, As_s, np.arange(S * k))
+    assert np.array_equal(gu.bits(Y.index_select(0, rows)), Y_ref)
+    got = gu.bits(out[torch.from_numpy(toks).cuda()])
+    gu.assert_close_bf16(got, oracle.combine(Y_ref, np.arange(S * k), w[toks]), "combine")
+    deq = (oracle.e4m3_decode(q).reshape(S, -1, 128) * s.astype(np.float64)[:, :, None]).reshape(S, -1)
+    gu.assert_close_bf16(got, oracle.f64_to_bf16(deq), "dispatch->identity->combine")

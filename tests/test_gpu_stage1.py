@@ -112,12 +112,24 @@ def test_stage1_wide_rows():
         P.check_same_as_unfused(opts)
 
 
-@pytest.mark.parametrize("name", ["t8192_zipf1.2"])
-def test_stage1_full_size_bit_identical_to_unfused(name):
-    P = Problem(inputs.CONFIGS[name])
+def test_stage1_full_size_bit_identical_to_unfused():
+    # the benchmark's step configuration and two others at T=8192
+    P = Problem(inputs.CONFIGS["t8192_zipf1.2"])
     for opts in (moe.stage1_opts(), moe.stage1_opts(comm_sms=24, schedule=moe.MOE_SCHED_READY_FIRST),
                  moe.stage1_opts(comm_sms=8, flags=moe.MOE_FLAGS_PER_EXPERT, producers_join=0)):
         P.check_same_as_unfused(opts)
+
+
+def test_stage1_t16384_sweep_configurations_bit_identical_to_unfused():
+    # the fused-stage1 sweep's workload (T=16384, Zipf 1.0): every producer SM
+    # count it times, across both flag granularities and both schedules
+    P = Problem(inputs.CONFIGS["stage1_t16384_zipf1.0"])
+    for comm, flags, schedule in [(8, moe.MOE_FLAGS_PER_TILE, moe.MOE_SCHED_EXPERT_MAJOR),
+                                  (16, moe.MOE_FLAGS_PER_EXPERT, moe.MOE_SCHED_READY_FIRST),
+                                  (24, moe.MOE_FLAGS_PER_TILE, moe.MOE_SCHED_READY_FIRST),
+                                  (36, moe.MOE_FLAGS_PER_EXPERT, moe.MOE_SCHED_EXPERT_MAJOR),
+                                  (36, moe.MOE_FLAGS_PER_TILE, moe.MOE_SCHED_EXPERT_MAJOR)]:
+        P.check_same_as_unfused(moe.stage1_opts(comm_sms=comm, flags=flags, schedule=schedule))
 
 
 @pytest.mark.parametrize("schedule", [moe.MOE_SCHED_EXPERT_MAJOR, moe.MOE_SCHED_READY_FIRST])
