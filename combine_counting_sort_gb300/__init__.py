@@ -110,6 +110,25 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _shape(t: Optional[torch.Tensor], want, name: str):
+    """Refuse a tensor whose shape is not the one the call's sizes imply: the C
+    entry points take bare device pointers, so a short buffer would be overrun
+    on the device instead of failing here."""
+    if t is not None and tuple(t.shape) != tuple(int(v) for v in want):
+        raise ValueError(f"{name} must have shape {tuple(int(v) for v in want)}, got {tuple(t.shape)}")
+
+
+def _status(t: torch.Tensor):
+    if t.numel() < 1:
+        raise ValueError("status must hold one int32")
+
+
+def _dims(t: torch.Tensor, n: int, name: str):
+    if t.dim() != n:
+        raise ValueError(f"{name} must have {n} dimensions, got {t.dim()}")
+    return tuple(t.shape)
+
+
 def _stream(stream) -> ctypes.c_void_p:
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
@@ -152,6 +171,9 @@ class Layout:
 
 def moe_route_layout(topk_ids: torch.Tensor, topk_w: torch.Tensor, layout: Layout, status: torch.Tensor,
                      stream=None):
+    _shape(topk_ids, (layout.T, layout.k), "topk_ids")
+    _shape(topk_w, (layout.T, layout.k), "topk_w")
+    _status(status)
     _check("moe_route_layout", lib().moe_route_layout(
         _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(topk_w, torch.float32, "topk_w"), ctypes.byref(layout.c),
         _ptr(layout.ws), layout.ws.numel(), _ptr(status, torch.int32, "status"), _stream(stream)))
@@ -162,6 +184,9 @@ def moe_route_layout_noalloc(topk_ids: torch.Tensor, topk_w: torch.Tensor, layou
     """moe_route_layout without a workspace: for callers that cannot allocate
     device memory, the scratch is a fixed array inside the library (E <= 256).
     Calls that can overlap on the GPU share that array and must be ordered."""
+    _shape(topk_ids, (layout.T, layout.k), "topk_ids")
+    _shape(topk_w, (layout.T, layout.k), "topk_w")
+    _status(status)
     _check("moe_route_layout_noalloc", lib().moe_route_layout_noalloc(
         _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(topk_w, torch.float32, "topk_w"), ctypes.byref(layout.c),
         _ptr(status, torch.int32, "status"), _stream(stream)))
@@ -169,6 +194,12 @@ def moe_route_layout_noalloc(topk_ids: torch.Tensor, topk_w: torch.Tensor, layou
 
 def moe_dispatch_quant(x: torch.Tensor, layout: Layout, A: torch.Tensor, A_scale: torch.Tensor,
                        status: torch.Tensor, stream=None):
+    T, H = _dims(x, 2, "x")
+    R = layout.T * layout.k
+    _shape(x, (layout.T, H), "x")
+    _shape(A, (R, H), "A")
+    _shape(A_scale, (H // 128, R), "A_scale")
+    _status(status)
     _check("moe_dispatch_quant", lib().moe_dispatch_quant(
         _ptr(x, torch.bfloat16, "x"), x.shape[1], ctypes.byref(layout.c), _ptr(A, torch.uint8, "A"),
         _ptr(A_scale, torch.float32, "A_scale"), _ptr(status, torch.int32, "status"), _stream(stream)))
@@ -176,7 +207,14 @@ def moe_dispatch_quant(x: torch.Tensor, layout: Layout, A: torch.Tensor, A_scale
 
 def moe_grouped_gemm1(A: torch.Tensor, A_scale: torch.Tensor, W: torch.Tensor, W_scale: torch.Tensor,
                       layout: Layout, Y: torch.Tensor, status: torch.Tensor, stream=None):
-    E, N, H = W.shape
+    E, N, H = _dims(W, 3, "W")
+    R = layout.T * layout.k
+    _shape(W, (layout.E, N, H), "W")
+    _shape(W_scale, (layout.E, N // 128, H // 128), "W_scale")
+    _shape(A, (R, H), "A")
+    _shape(A_scale, (H // 128, R), "A_scale")
+    _shape(Y, (R, N), "Y")
+    _status(status)
     _check("moe_grouped_gemm1", lib().moe_grouped_gemm1(
         _ptr(A, torch.uint8, "A"), _ptr(A_scale, torch.float32, "A_scale"), _ptr(W, torch.uint8, "W"),
         _ptr(W_scale, torch.float32, "W_scale"), N, H, ctypes.byref(layout.c), _ptr(Y, torch.bfloat16, "Y"),
@@ -184,6 +222,10 @@ def moe_grouped_gemm1(A: torch.Tensor, A_scale: torch.Tensor, W: torch.Tensor, W
 
 
 def moe_combine(Y: torch.Tensor, layout: Layout, out: torch.Tensor, status: torch.Tensor, stream=None):
+    _, D = _dims(Y, 2, "Y")
+    _shape(Y, (layout.T * layout.k, D), "Y")
+    _shape(out, (layout.T, D), "out")
+    _status(status)
     _check("moe_combine", lib().moe_combine(
         _ptr(Y, torch.bfloat16, "Y"), Y.shape[1], ctypes.byref(layout.c), _ptr(out, torch.bfloat16, "out"),
         _ptr(status, torch.int32, "status"), _stream(stream)))
@@ -211,7 +253,15 @@ def stage1_trace(ws: torch.Tensor) -> dict:
 def moe_stage1(x: torch.Tensor, layout: Layout, W: torch.Tensor, W_scale: torch.Tensor, A: torch.Tensor,
                A_scale: torch.Tensor, Y: torch.Tensor, ws: torch.Tensor, status: torch.Tensor,
                opts: Optional[Stage1Opts] = None, stream=None):
-    E, N, H = W.shape
+    E, N, H = _dims(W, 3, "W")
+    R = layout.T * layout.k
+    _shape(x, (layout.T, H), "x")
+    _shape(W, (layout.E, N, H), "W")
+    _shape(W_scale, (layout.E, N // 128, H // 128), "W_scale")
+    _shape(A, (R, H), "A")
+    _shape(A_scale, (H // 128, R), "A_scale")
+    _shape(Y, (R, N), "Y")
+    _status(status)
     opts = stage1_opts() if opts is None else opts
     _check("moe_stage1", lib().moe_stage1(
         _ptr(x, torch.bfloat16, "x"), H, ctypes.byref(layout.c), _ptr(W, torch.uint8, "W"),
@@ -221,20 +271,29 @@ def moe_stage1(x: torch.Tensor, layout: Layout, W: torch.Tensor, W_scale: torch.
 
 
 def moe_router_topk(logits: torch.Tensor, k: int, topk_ids: torch.Tensor, topk_w: torch.Tensor, stream=None):
-    T, E = logits.shape
+    T, E = _dims(logits, 2, "logits")
+    _shape(topk_ids, (T, k), "topk_ids")
+    _shape(topk_w, (T, k), "topk_w")
     _check("moe_router_topk", lib().moe_router_topk(
         _ptr(logits, torch.float32, "logits"), T, E, k, _ptr(topk_ids, torch.int32, "topk_ids"),
         _ptr(topk_w, torch.float32, "topk_w"), _stream(stream)))
 
 
 def moe_quant_weights(W: torch.Tensor, Wq: torch.Tensor, W_scale: torch.Tensor, stream=None):
-    E, N, H = W.shape
+    E, N, H = _dims(W, 3, "W")
+    _shape(Wq, (E, N, H), "Wq")
+    _shape(W_scale, (E, N // 128, H // 128), "W_scale")
     _check("moe_quant_weights", lib().moe_quant_weights(
         _ptr(W, torch.bfloat16, "W"), E, N, H, _ptr(Wq, torch.uint8, "Wq"),
         _ptr(W_scale, torch.float32, "W_scale"), _stream(stream)))
 
 
 def moe_dequant_rows(A: torch.Tensor, A_scale: torch.Tensor, layout: Layout, Y: torch.Tensor, stream=None):
+    _, H = _dims(A, 2, "A")
+    R = layout.T * layout.k
+    _shape(A, (R, H), "A")
+    _shape(A_scale, (H // 128, R), "A_scale")
+    _shape(Y, (R, H), "Y")
     _check("moe_dequant_rows", lib().moe_dequant_rows(
         _ptr(A, torch.uint8, "A"), _ptr(A_scale, torch.float32, "A_scale"), A.shape[1], ctypes.byref(layout.c),
         _ptr(Y, torch.bfloat16, "Y"), _stream(stream)))

@@ -61,17 +61,19 @@ inline bool device_has_tcgen05() {
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against libcuda, so the library loads on machines without a driver).
+// against libcuda, so the library loads on machines without a driver).  Looked
+// up once, by the first call that needs it (a thread-safe static initialiser);
+// null where there is no driver, and the entry points then return MOE_ERR_CUDA.
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+  }();
   return fn;
 }
 

@@ -7,6 +7,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 import combine_counting_sort_gb300 as moe
 import oracle
@@ -99,3 +100,44 @@ def test_ctypes_structs_match_header(tmp_path):
     want = [ctypes.sizeof(moe.LayoutC), moe.LayoutC.count.offset, moe.LayoutC.token_order.offset,
             ctypes.sizeof(moe.LayoutSizes), ctypes.sizeof(moe.Stage1Opts), moe.Stage1Opts.timeout_ns.offset]
     assert got == want
+
+
+def test_binding_refuses_wrong_shapes_before_any_device_call(lib):
+    # The C entry points take bare pointers; the binding checks every tensor's
+    # shape against the layout and the other operands first (CPU tensors here:
+    # a shape error comes before the device check, a right shape reaches it).
+    T, k, E, G, H, N = 40, 2, 8, 2, 256, 512
+    R = T * k
+    L = moe.Layout(T, k, E, G, device="cpu")
+    st = torch.zeros(1, dtype=torch.int32)
+    u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+    x = torch.zeros(T, H, dtype=bf)
+    A, As = torch.zeros(R, H, dtype=u8), torch.zeros(H // 128, R, dtype=f32)
+    W, Ws = torch.zeros(E, N, H, dtype=u8), torch.zeros(E, N // 128, H // 128, dtype=f32)
+    Y, out = torch.zeros(R, N, dtype=bf), torch.zeros(T, N, dtype=bf)
+    bad = [
+        lambda: moe.moe_route_layout(torch.zeros(T, k + 1, dtype=torch.int32), torch.zeros(T, k), L, st),
+        lambda: moe.moe_route_layout_noalloc(torch.zeros(T, k, dtype=torch.int32), torch.zeros(T - 1, k), L, st),
+        lambda: moe.moe_dispatch_quant(torch.zeros(T + 1, H, dtype=bf), L, A, As, st),
+        lambda: moe.moe_dispatch_quant(x, L, A[:-1], As, st),
+        lambda: moe.moe_dispatch_quant(x, L, A, As[:, :-1], st),
+        lambda: moe.moe_grouped_gemm1(A, As, W[:-1], Ws[:-1], L, Y, st),
+        lambda: moe.moe_grouped_gemm1(A, As, W, Ws[:, :-1], L, Y, st),
+        lambda: moe.moe_grouped_gemm1(A, As, W, Ws, L, Y[:-1], st),
+        lambda: moe.moe_combine(Y, L, out[:-1], st),
+        lambda: moe.moe_combine(Y[:-1], L, out, st),
+        lambda: moe.moe_stage1(x, L, W, Ws, A, As, Y[:, :-128], torch.zeros(16, dtype=u8), st),
+        lambda: moe.moe_router_topk(torch.zeros(T, E), k, torch.zeros(T, k + 1, dtype=torch.int32),
+                                    torch.zeros(T, k + 1)),
+        lambda: moe.moe_quant_weights(torch.zeros(E, N, H, dtype=bf), W[:, :-1], Ws),
+        lambda: moe.moe_dequant_rows(A, As, L, torch.zeros(R, H + 128, dtype=bf)),
+        lambda: moe.moe_combine(Y, L, out, torch.zeros(0, dtype=torch.int32)),
+    ]
+    for call in bad:
+        with pytest.raises(ValueError, match="shape|dimensions|status"):
+            call()
+    # right shapes pass the shape checks and stop at the device check
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        moe.moe_grouped_gemm1(A, As, W, Ws, L, Y, st)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        moe.moe_combine(Y, L, out, st)
