@@ -118,7 +118,10 @@ typedef struct moe_layout {
  *   topk_w    device f32 [T, k] router weights (copied to row_weight).
  *   ws        device workspace of at least layout_ws_bytes (contents ignored;
  *             the call initialises what it uses, in-stream).
- * One launch (a cooperative grid with one grid-wide barrier). */
+ * One launch: a cooperative grid of at most one block per SM with two
+ * grid-wide barriers (each bounded: a barrier not reached within 1 s writes
+ * MOE_ERR_TIMEOUT to *status and the kernel returns), or, for T <= 32, a
+ * single block in a plain launch with neither. */
 int moe_route_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
                      void* ws, size_t ws_bytes, int32_t* status, moe_stream_t stream);
 
