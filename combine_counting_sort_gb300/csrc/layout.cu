@@ -4,21 +4,23 @@
 // The counting sort of the mori stage1 page ("How it works now": a counting
 // sort by (destination, first expert) so that a landed prefix of a run is a
 // prefix of experts; recv_layout commit: per-expert counts, padding of every
-// expert to the sort block, expert-major tables) as ONE cooperative launch:
+// expert to the sort block, expert-major tables) as ONE launch: a cooperative
+// grid of at most one block per SM (T <= 32: a single block in a plain launch,
+// which needs neither barrier):
 //
 //   phase A  each block histograms its contiguous token range: experts of its
 //            pairs and first (smallest) experts of its tokens, with
 //            warp-aggregated shared-memory adds (__match_any_sync leaders);
 //            the block's ids and weights stay staged in shared memory.
-//   barrier  grid-wide barrier (bounded spin).
+//   barrier  grid-wide barrier (bounded spin: MOE_ERR_TIMEOUT after 1 s).
 //   phase B  the per-block histograms are scanned down the blocks, one warp
 //            per expert column (in place: each entry becomes that block's
 //            exclusive prefix; the column total goes to a totals array);
 //            after a second grid barrier every block reads its own row of
 //            prefixes and the totals, scans across experts (expert offsets,
 //            tile offsets, first-expert offsets) in shared memory; block 0
-//            writes the E-sized tables, all blocks write tile tables and the
-//            rowmap grid-stride.
+//            writes the E-sized tables; the tile tables and the rowmap are
+//            written one tile per warp over the whole grid.
 //   phase C  stable ranks: the block's pairs, in (token, slot) order, are cut
 //            into one contiguous slice per warp; per-warp histograms scanned
 //            across the warps give each warp its first row per expert, and each

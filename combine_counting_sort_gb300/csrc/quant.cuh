@@ -3,7 +3,9 @@
 //
 // ("How it works now" and the quant-once commit of the mori stage1 page: a
 // token's bf16 row is read and quantised once and stored to its row in every
-// run it belongs to.)  One warp per token.  A lane owns 16 consecutive values
+// run it belongs to.)  A warp quantises a slice of 512 x ROUNDS columns of one
+// token at a time (the dispatch kernel splits a token's row into slices over
+// several warps; a fused-stage1 producer warp walks whole tokens).  A lane owns 16 consecutive values
 // (two 16-byte loads), so a 128-value quantisation block is 8 lanes and a warp
 // round covers 512 values; the block amax is a 3-step xor-shuffle reduction.
 // The 16 codes of a lane are one 16-byte store, so a warp's store covers 512

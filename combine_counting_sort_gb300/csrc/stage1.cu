@@ -14,13 +14,19 @@
 // bounded waits below safe):
 //   CTAs [0, S)   producers: every warp quantises tokens taken in token_order
 //                 (tokens sorted by first expert, so rows of low experts land
-//                 first), stores codes and scales to the token's k rows, then
-//                 publishes each row with a release add on its tile's flag
-//                 (or its expert's flag).  With producers_join they then take
-//                 GEMM work like the consumers.
-//   CTAs [S, #SM) consumers: the GEMM1 pipeline of gemm1.cuh; the TMA thread
-//                 acquires a unit's ready flag (bounded wait) before its first
-//                 load, and so do the epilogue warps before reading A_scale.
+//                 first) into one of two shared-memory row buffers, stores the
+//                 block scales to the token's k rows and bulk-copies the code
+//                 row to each of them; once a token's copies are complete (one
+//                 token later) each of its rows is published with a release
+//                 add on its tile's flag (or its expert's flag).  Rows too wide
+//                 for two buffers per warp go out by 16-byte stores instead.
+//                 With producers_join they then take GEMM work like the
+//                 consumers.
+//   CTAs [S, #SM) consumers: the GEMM1 pipeline of gemm1.cuh; the TMA warp
+//                 acquires a unit's ready flag (bounded wait) before it hands
+//                 the unit to the MMA and promotion warps and before the
+//                 unit's first load; the unit ring's mbarrier carries that
+//                 acquire on to the promotion warps' A_scale reads.
 // Units come from a static expert-major stride, or from a global ticket
 // counter (expert-major order, or positions of the ready queue filled by a
 // scheduler warp in readiness order).
