@@ -28,7 +28,7 @@ router softmax, the dequantised matmul, the weighted combine) is computed in
 fp64 and rounded once to the output format; the pages leave that precision
 open.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * top-k ties go to the lower expert id; a token's slots are ordered by
   descending probability;
