@@ -342,7 +342,9 @@ def grouped_gemm1(A, A_scale, Wq, W_scale, expert_offset, rows=None):
 def combine(Y_bits: np.ndarray, pair_row: np.ndarray, topk_w: np.ndarray, tokens=None):
     """out[t] = bf16( sum_{j=0}^{k-1} w[t, j] * Y[pair_row[t*k + j]] ) in fp64,
     slots in ascending order: the weighted gather of each token's k expert
-    outputs back into token order.
+    outputs back into token order ([tilepipe] "Communication Kernels" names the
+    combine as the counterpart of the dispatch; the router weighting and the
+    fp64 accumulation in slot order are this oracle's reading).
 
     Returns bf16 bit patterns [len(tokens), D]."""
     w = np.asarray(topk_w, dtype=np.float32)
