@@ -355,3 +355,54 @@ def combine(Y_bits: np.ndarray, pair_row: np.ndarray, topk_w: np.ndarray, tokens
     for j in range(k):
         acc += w[tokens, j].astype(np.float64)[:, None] * bf16_to_f32(Y_bits[rows[:, j]]).astype(np.float64)
     return f64_to_bf16(acc)
+
+
+# --------------------------------------------------------------------------
+# Per-(token, group) send runs (the next step of the path: no CUDA kernel reads
+# these yet; the dense dispatch above is what the kernels compute)
+# --------------------------------------------------------------------------
+
+def group_runs(topk_ids: np.ndarray, E: int, G: int, row_pair: np.ndarray):
+    """One send row per (token, logical group) that the token routes into,
+    the rows of group g forming run g ([mori] "What": the sender quantises each
+    token once into a send buffer grouped by destination; "How it works now":
+    a counting sort by (destination, first expert) places every token's row
+    so that a landed prefix of a run is a prefix of experts).  Within run g
+    rows follow (the token's smallest expert id in g, token).  GEMM1 would read
+    dense expert-major row r (pair p = row_pair[r] of token t = p // k, expert
+    e) from send row ``send_row[t, e // (E/G)]``: ``gather_row[r]``.
+
+    Returns a dict: run_offset [G+1]; send_token [S] (token of each send row);
+    send_row [T, G] (-1 where the token has no route into g); run_ready [E]
+    (for expert e of group g, the end of the run prefix that holds every token
+    routed to e); gather_row [T*k]."""
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    T, k = ids.shape
+    assert E % G == 0
+    epg = E // G
+    grp = ids // epg
+    send_row = np.full((T, G), -1, np.int64)
+    run_offset = np.zeros(G + 1, np.int64)
+    run_ready = np.zeros(E, np.int64)
+    send_token = []
+    for g in range(G):
+        in_g = grp == g
+        toks = np.nonzero(in_g.any(axis=1))[0]
+        first = np.where(in_g, ids, E).min(axis=1)[toks]       # smallest expert of g per token
+        order = toks[np.argsort(first, kind="stable")]
+        run_offset[g + 1] = run_offset[g] + len(order)
+        send_row[order, g] = run_offset[g] + np.arange(len(order))
+        send_token.append(order)
+        run_ready[g * epg:(g + 1) * epg] = run_offset[g] + np.cumsum(np.bincount(first - g * epg, minlength=epg))
+    rp = np.asarray(row_pair, dtype=np.int64)
+    gather_row = send_row[rp // k, ids.reshape(-1)[rp] // epg]
+    i32 = lambda a: np.asarray(a, dtype=np.int32)
+    return {"run_offset": i32(run_offset), "send_token": i32(np.concatenate(send_token)),
+            "send_row": i32(send_row), "run_ready": i32(run_ready), "gather_row": i32(gather_row)}
+
+
+def dispatch_runs(q: np.ndarray, scale: np.ndarray, send_token: np.ndarray):
+    """The send buffer: each send row holds its token's codes once, scales
+    block-major as in ``dispatch`` (A_send [S, H], A_send_scale [H/128, S])."""
+    st = np.asarray(send_token, dtype=np.int64)
+    return q[st].copy(), np.ascontiguousarray(scale[st].T)

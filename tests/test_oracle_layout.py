@@ -189,3 +189,77 @@ def test_router_weights_are_softmax_of_selected_logits():
     # shift invariance
     ids2, w2 = oracle.router_topk(logits + np.float32(5.0), 4)
     assert np.array_equal(ids, ids2) and np.allclose(w, w2, rtol=1e-6)
+
+
+# ---- per-(token, group) send runs (the next step of the path)
+
+def brute_runs(ids, E, G):
+    """Send rows by direct enumeration: Python sort of (group, first expert of
+    the token in the group, token) over the tokens with a route into the group."""
+    T, k = ids.shape
+    epg = E // G
+    keys = sorted((g, min(int(e) for e in ids[t] if int(e) // epg == g), t)
+                  for t in range(T) for g in range(G) if any(int(e) // epg == g for e in ids[t]))
+    send_row = {(t, g): s for s, (g, _, t) in enumerate(keys)}
+    run_offset = [sum(1 for g2, _, _ in keys if g2 < g) for g in range(G + 1)]
+    return keys, send_row, run_offset
+
+
+@pytest.mark.parametrize("T,k,E,G,seed", [(1, 1, 1, 1, 0), (9, 3, 6, 3, 1), (25, 4, 8, 2, 2), (40, 6, 12, 4, 3),
+                                         (30, 5, 5, 1, 4), (17, 4, 16, 16, 5)])
+def test_group_runs_brute_force(T, k, E, G, seed):
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)           # duplicates allowed
+    L = oracle.route_layout(ids, np.ones((T, k), np.float32), E, G)
+    out = oracle.group_runs(ids, E, G, L["row_pair"])
+    keys, send_row, run_offset = brute_runs(ids, E, G)
+    assert list(out["run_offset"]) == run_offset
+    assert list(out["send_token"]) == [t for _, _, t in keys]
+    for t in range(T):
+        for g in range(G):
+            assert out["send_row"][t, g] == send_row.get((t, g), -1)
+    epg = E // G
+    for r, p in enumerate(L["row_pair"]):
+        t, e = p // k, int(ids.reshape(-1)[p])
+        assert out["gather_row"][r] == send_row[(t, e // epg)]
+
+
+@pytest.mark.parametrize("name", ["tiny", "t2048_uniform", "t8192_zipf1.2"])
+def test_group_runs_invariants_on_workloads(name):
+    cfg = inputs.CONFIGS[name]
+    logits = inputs.make_logits(cfg.T, cfg.E, cfg.zipf, cfg.seed).numpy()
+    ids, w = oracle.router_topk(logits, cfg.k)
+    L = oracle.route_layout(ids, w, cfg.E, cfg.G)
+    out = oracle.group_runs(ids, cfg.E, cfg.G, L["row_pair"])
+    epg = cfg.E // cfg.G
+    grp = ids.astype(np.int64) // epg
+    # one send row per (token, group) with a route into the group, and no other
+    pairs = {(t, g) for t in range(cfg.T) for g in set(grp[t].tolist())}
+    S = int(out["run_offset"][-1])
+    assert S == len(pairs) == len(out["send_token"]) and S <= cfg.T * cfg.k
+    assert sorted(out["send_row"][out["send_row"] >= 0].tolist()) == list(range(S))
+    # every dense row gathers a send row of its own token
+    tok_of_row = L["row_pair"] // cfg.k
+    assert np.array_equal(out["send_token"][out["gather_row"]], tok_of_row)
+    # a landed prefix of a run is a prefix of experts: every token routed to
+    # expert e sits before run_ready[e] in its group's run
+    for e in range(cfg.E):
+        rows = out["gather_row"][L["expert_offset"][e]:L["expert_offset"][e + 1]]
+        assert np.all(rows < out["run_ready"][e])
+        assert np.all(rows >= out["run_offset"][e // epg])
+    assert np.all(np.diff(out["run_ready"].reshape(cfg.G, epg), axis=1) >= 0)
+
+
+def test_send_runs_gather_reproduces_the_dense_dispatch():
+    # reading A through gather_row gives the dense dispatch buffer bit for bit
+    cfg = inputs.MoEConfig("runs", T=300, H=512, E=32, G=4, k=6, N=256, zipf=1.2, seed=7)
+    logits = inputs.make_logits(cfg.T, cfg.E, cfg.zipf, cfg.seed).numpy()
+    ids, w = oracle.router_topk(logits, cfg.k)
+    L = oracle.route_layout(ids, w, cfg.E, cfg.G)
+    q, s = oracle.quantize_rows(inputs.bf16_bits(inputs.make_x(cfg.T, cfg.H, cfg.seed)))
+    A, As = oracle.dispatch(q, s, L["pair_row"], cfg.k)
+    R = oracle.group_runs(ids, cfg.E, cfg.G, L["row_pair"])
+    A_send, As_send = oracle.dispatch_runs(q, s, R["send_token"])
+    assert np.array_equal(A_send[R["gather_row"]], A)
+    assert np.array_equal(As_send[:, R["gather_row"]].view(np.uint32), As.view(np.uint32))
+    assert A_send.shape[0] < A.shape[0]
