@@ -87,6 +87,81 @@ def test_quant_tiny_blocks_with_subnormal_scales():
     assert np.all(q[3, :128] == 0x7E)
 
 
+def _brute_e4m3(v: "Fraction") -> int:
+    """e4m3 code of an exact rational by direct search: the nearest of the 127
+    non-negative grid values (3 mantissa bits, exponent bias 7, subnormal step
+    2**-9), ties to the even code, magnitudes above 448 saturated; sign from v."""
+    from fractions import Fraction
+    grid = [Fraction(8 + m, 8) * Fraction(2) ** (e - 7) if e else Fraction(m, 512)
+            for e in range(16) for m in range(8)][:127]
+    a = min(abs(v), Fraction(448))
+    best = min(range(127), key=lambda c: (abs(grid[c] - a), c & 1))
+    return best | (0x80 if v < 0 else 0)
+
+
+def _fp32_of(v: "Fraction") -> "Fraction":
+    """Round an exact rational to the nearest fp32 value (ties to even), by
+    integer arithmetic on the 24-bit significand (normal range)."""
+    from fractions import Fraction
+    if v == 0:
+        return Fraction(0)
+    sign, a = (-1 if v < 0 else 1), abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    scaled = a / Fraction(2) ** (e - 23)                   # in [2**23, 2**24)
+    n, rem = divmod(scaled.numerator, scaled.denominator)
+    twice = 2 * rem
+    if twice > scaled.denominator or (twice == scaled.denominator and n & 1):
+        n += 1
+    return sign * Fraction(n) * Fraction(2) ** (e - 23)
+
+
+def test_quant_codes_are_the_e4m3_rounding_of_the_ieee_quotient():
+    # For a few block maxima, every bf16 value of [-amax, amax] in one block
+    # each: the code must be the e4m3 rounding of RN_fp32(x / scale) with
+    # scale = RN_fp32(amax / 448), here computed in exact rational arithmetic
+    # with a brute-force nearest-code search for the values whose quotient lies
+    # near an e4m3 rounding boundary, and for the rest through float64 (a
+    # quotient of fp32 operands rounded once to float64 and again to float32 is
+    # rounded correctly).  A reciprocal shortcut x * RN(1/scale) fails.
+    from fractions import Fraction
+    rng = np.random.default_rng(17)
+    amaxes = [7.0 / 3.0, 0.1, 13.7, 1e4, 3.0, 1.0]
+    amaxes += list(oracle.bf16_to_f32(rng.integers(0x3C00, 0x4600, 16).astype(np.uint16)).astype(np.float64))
+    bad_shortcut, checked = 0, 0
+    for a in amaxes:
+        ab = oracle.f64_to_bf16(np.array([a]))[0]
+        pos = np.arange(0, int(ab) + 1, dtype=np.uint32).astype(np.uint16)
+        vals = np.concatenate([pos, pos | np.uint16(0x8000)])
+        nb = (len(vals) + 126) // 127
+        blocks = np.concatenate([vals, np.zeros(nb * 127 - len(vals), np.uint16)]).reshape(nb, 127)
+        xb = np.concatenate([np.full((nb, 1), ab, np.uint16), blocks], axis=1).reshape(1, -1)
+        q, s = oracle.quantize_rows(xb)
+        scale = np.float32(s[0, 0])
+        assert np.all(s == scale)
+        assert Fraction(float(scale)) == _fp32_of(Fraction(float(oracle.bf16_to_f32(np.array([ab]))[0])) / 448)
+        xf = oracle.bf16_to_f32(xb[0])
+        quot = (xf.astype(np.float64) / np.float64(scale)).astype(np.float32)
+        assert np.array_equal(q[0], oracle.e4m3_encode(quot))
+        # the delicate values: quotients within 2**-20 (relative) of an e4m3 midpoint
+        grid = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+        mids = (grid[1:] + grid[:-1]) / 2
+        aq = np.abs(xf.astype(np.float64) / float(scale))
+        near = np.nonzero(np.min(np.abs(aq[:, None] - mids[None, :]) / np.maximum(mids[None, :], 1e-30), axis=1)
+                          < 2.0 ** -20)[0]
+        for i in near[:400]:
+            exact = _fp32_of(Fraction(float(xf[i])) / Fraction(float(scale)))
+            assert q[0, i] == _brute_e4m3(exact), (a, i)
+            checked += 1
+        short = oracle.e4m3_encode((xf * (np.float32(1) / scale)).astype(np.float32))
+        bad_shortcut += int(np.count_nonzero(short != q[0]))
+    assert checked >= 100            # quotients at or next to a rounding midpoint were checked exactly
+    assert bad_shortcut > 0          # the pin tells the IEEE quotient from the reciprocal shortcut
+
+
 def test_dispatch_places_every_copy():
     cfg = inputs.CONFIGS["tiny"]
     x = inputs.bf16_bits(inputs.make_x(cfg.T, cfg.H))
