@@ -1,6 +1,7 @@
-"""The benchmark's reference arm (the CPU oracle on the host cores): its JSON
-line, its sampler's coverage of the experts, and that ranks other than 0 do
-no work.  CPU only."""
+"""The benchmark's host-side logic, on the CPU: the reference arm (the CPU
+oracle on the host cores: its JSON line, its sampler's coverage of the
+experts, ranks other than 0 doing no work), the key of the stored DRAM
+traffic figure, and the warm-up rule."""
 import json
 import os
 import subprocess
@@ -56,3 +57,26 @@ def test_sampler_times_every_nonempty_expert_once_before_repeating():
     # with every expert timed once, the GEMM1 part of the estimate is their sum
     gemm_ms = s.step_ms() - 1e3 * s.t_fixed[0]
     assert abs(gemm_ms - 1e3 * sum(s.t_experts)) <= 1e-6 * gemm_ms
+
+
+def test_traffic_key_follows_kernel_code_not_comments(tmp_path, monkeypatch):
+    # the DRAM-traffic figure is keyed by a hash of the kernel sources' code:
+    # editing a comment keeps it, editing code drops it (null until recaptured)
+    import shutil
+    src = os.path.join(ROOT, "combine_counting_sort_gb300", "csrc")
+    fake_root = tmp_path / "root"
+    shutil.copytree(src, fake_root / "combine_counting_sort_gb300" / "csrc")
+    monkeypatch.setattr(bench, "ROOT", str(fake_root))
+    h0 = bench.kernel_source_hash()
+    f = fake_root / "combine_counting_sort_gb300" / "csrc" / "stage1.cu"
+    text = f.read_text()
+    f.write_text(text + "\n// a comment\n/* another\n comment */\n")
+    assert bench.kernel_source_hash() == h0
+    f.write_text(text.replace("kGemmStages", "kGemmStages ", 1) + "\nstatic int unused_probe;\n")
+    assert bench.kernel_source_hash() != h0
+
+
+def test_bench_refuses_fewer_than_three_warmup_steps():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"], capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode != 0 and "warmup" in r.stderr
