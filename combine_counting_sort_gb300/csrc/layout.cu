@@ -555,16 +555,23 @@ static __device__ __align__(256) unsigned char g_layout_scratch[moe::kNoAllocScr
 
 #include <mutex>
 
-// Device address of g_layout_scratch on each device, looked up once per device
-// (the symbol's name is only a host-side handle; kernels need this address).
+// Device address of g_layout_scratch on each device (the symbol's name is only
+// a host-side handle; kernels need this address).  Looked up again on every
+// call made outside a stream capture, so a context torn down and created again
+// (cudaDeviceReset) gets the new address; a call inside a capture uses the
+// address of the last uncaptured call on that device, and the very first call
+// on a device must not be inside a capture.
 static void* g_scratch_addr[128];
 static std::mutex g_scratch_mu;
 
-static int layout_scratch_address(void** out) {
+static int layout_scratch_address(cudaStream_t s, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return MOE_ERR_CUDA;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone || !g_scratch_addr[dev]) {
+    if (cap != cudaStreamCaptureStatusNone) return MOE_ERR_CUDA;   // first call inside a capture
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_layout_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
     g_scratch_addr[dev] = p;
@@ -580,7 +587,7 @@ extern "C" int moe_route_layout_noalloc(const int32_t* topk_ids, const float* to
   if (!topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if (L->E > kNoAllocMaxExperts) return MOE_ERR_UNSUPPORTED;   // beyond the fixed scratch
   void* ws = nullptr;
-  rc = layout_scratch_address(&ws);
+  rc = layout_scratch_address((cudaStream_t)stream, &ws);
   if (rc) return rc;
   return launch_layout(topk_ids, topk_w, L, ws, status, (cudaStream_t)stream);
 }

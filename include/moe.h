@@ -136,8 +136,12 @@ int moe_route_layout(const int32_t* topk_ids, const float* topk_w, const moe_lay
  *   Limit: E <= MOE_NOALLOC_MAX_EXPERTS (larger E returns MOE_ERR_UNSUPPORTED);
  *   other limits and outputs as moe_route_layout.
  *   The array (about 512 KiB) is reserved on every GPU that loads the library
- *   until the process exits.  The first call on each device looks up the
- *   array's device address; make that first call outside any stream capture.
+ *   until the process exits.  Every call made outside a stream capture looks
+ *   up the array's device address (so a context reset is followed); a call
+ *   inside a capture reuses the address of the last uncaptured call on that
+ *   device, so make the first call on each device (and the first one after a
+ *   cudaDeviceReset) outside any stream capture: a first call inside a
+ *   capture returns MOE_ERR_CUDA.
  *   All calls share the one array: calls that can overlap on the GPU (other
  *   streams, other threads) race and must be ordered by the caller. */
 #define MOE_NOALLOC_MAX_EXPERTS 256

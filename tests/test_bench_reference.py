@@ -80,3 +80,14 @@ def test_bench_refuses_fewer_than_three_warmup_steps():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"], capture_output=True,
                        text=True, timeout=300)
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_roofline_peak_follows_the_timed_region():
+    # a short region at full clocks is measured against the burst peak; only a
+    # region long enough to hit the power cap, with the cap seen by
+    # nvidia-smi, is measured against the sustained peak
+    assert bench.roofline_peak_kind(0.047, {"reasons": []}) == "burst"
+    assert bench.roofline_peak_kind(0.047, {"reasons": ["sw_power_cap"]}) == "burst"
+    assert bench.roofline_peak_kind(1.2, {"reasons": []}) == "burst"
+    assert bench.roofline_peak_kind(1.2, {"reasons": ["sw_power_cap"]}) == "sustained"
+    assert bench.roofline_peak_kind(5.0, {"reasons": ["not sampled"]}) == "burst"
