@@ -43,7 +43,8 @@ Readings where the pages are silent:
   tile_rows = 0, and every rowmap slot not holding a row holds -1.
 
 Pins: every function here is checked by ``tests/test_oracle_*.py`` against
-brute force, closed forms, invariants or library routines; none is unpinned.
+brute force, closed forms, invariants or library routines; none is unpinned
+(the MXFP8 functions at the end by ``tests/test_oracle_mx.py``).
 """
 from __future__ import annotations
 
@@ -406,3 +407,111 @@ def dispatch_runs(q: np.ndarray, scale: np.ndarray, send_token: np.ndarray):
     block-major as in ``dispatch`` (A_send [S, H], A_send_scale [H/128, S])."""
     st = np.asarray(send_token, dtype=np.int64)
     return q[st].copy(), np.ascontiguousarray(scale[st].T)
+
+
+# --------------------------------------------------------------------------
+# MXFP8 variant: e8m0 (power-of-two) scales per 32 values
+# --------------------------------------------------------------------------
+#
+# [mori] (the stage1 page's first commit: "GEMM1 reads its A rows and e8m0
+# scales through a rowmap"; the quant-LDS commit packs "the e8m0 scales four
+# per dword") quantises with power-of-two scales.  The pages do not state the
+# block size or how the power of two is chosen.  Readings:
+#   * the block is 32 consecutive values along the reduction dimension (the
+#     OCP microscaling block; the tensor core's block-scaled FP8 MMA consumes
+#     one scale per 32 values), for activations and for each weight row alike;
+#   * the scale is the fp32 recipe's amax / 448 rounded UP to a power of two,
+#     2**X with X the smallest integer such that 448 * 2**X >= amax (so no
+#     value is pushed past 448 by the scale), clamped to the e8m0 range
+#     [-127, 127]; an all-zero block gets X = -127;
+#   * e8m0 code = X + 127 (0xFF, NaN, is never produced); codes of the values
+#     are e4m3(x / 2**X), round to nearest even, saturating.
+
+MX_BLOCK = 32
+E8M0_MIN_EXP, E8M0_MAX_EXP = -127, 127
+
+
+def mx_scale_exponent(amax: np.ndarray) -> np.ndarray:
+    """Smallest integer X with 448 * 2**X >= amax, clamped to [-127, 127]
+    (amax == 0 gives -127).  Exact: amax = m * 2**e with m in [0.5, 1)
+    (frexp), so 448 * 2**X = 0.875 * 2**(X + 9) >= m * 2**e holds for
+    X = e - 9 when m <= 0.875 and needs X = e - 8 otherwise."""
+    a = np.asarray(amax, dtype=np.float64)
+    m, e = np.frexp(a)
+    X = np.where(m <= 0.875, e - 9, e - 8).astype(np.int64)
+    X = np.where(a > 0, X, E8M0_MIN_EXP)
+    return np.clip(X, E8M0_MIN_EXP, E8M0_MAX_EXP)
+
+
+def e8m0_decode(codes: np.ndarray) -> np.ndarray:
+    """e8m0 code -> 2**(code - 127) (fp64); code 0xFF is NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    return np.where(c == 255, np.nan, np.ldexp(1.0, c - 127))
+
+
+def _mx_quantize_blocks(vals: np.ndarray):
+    """vals [..., nb, 32] float32 -> (codes uint8 same shape, e8m0 uint8 [..., nb])."""
+    amax = np.abs(vals).max(axis=-1)
+    X = mx_scale_exponent(amax)
+    scaled = (vals.astype(np.float64) * np.ldexp(1.0, -X)[..., None]).astype(np.float32)   # exact
+    return e4m3_encode(scaled), (X + 127).astype(np.uint8)
+
+
+def quantize_rows_mx(x_bits: np.ndarray):
+    """Per token and per 32-value block along H: X from the block's amax as
+    above, code = e4m3(x / 2**X).  x_bits: bf16 [T, H] -> (q uint8 [T, H],
+    e8m0 uint8 [T, H/32])."""
+    x = bf16_to_f32(x_bits)
+    T, H = x.shape
+    assert H % MX_BLOCK == 0
+    q, s = _mx_quantize_blocks(x.reshape(T, H // MX_BLOCK, MX_BLOCK))
+    return q.reshape(T, H), s
+
+
+def quantize_weights_mx(w_bits: np.ndarray):
+    """Expert weights bf16 [E, N, H] -> (codes uint8 [E, N, H], e8m0 uint8
+    [E, N, H/32]): one scale per weight row n and 32-value block along K."""
+    w = bf16_to_f32(w_bits)
+    E, N, H = w.shape
+    assert H % MX_BLOCK == 0
+    q, s = _mx_quantize_blocks(w.reshape(E, N, H // MX_BLOCK, MX_BLOCK))
+    return q.reshape(E, N, H), s
+
+
+def dequantize_mx(q: np.ndarray, e8m0: np.ndarray) -> np.ndarray:
+    """codes [..., H] and e8m0 scales [..., H/32] -> fp64 values (exact)."""
+    vals = e4m3_decode(q)
+    sh = vals.shape
+    v = vals.reshape(sh[:-1] + (sh[-1] // MX_BLOCK, MX_BLOCK)) * e8m0_decode(e8m0)[..., None]
+    return v.reshape(sh)
+
+
+def dispatch_mx(q: np.ndarray, e8m0: np.ndarray, pair_row: np.ndarray, k: int):
+    """The dispatch of the MX variant: token t's codes and e8m0 scales go to
+    each of its k dense rows pair_row[t*k + j], as in ``dispatch``.
+    Returns (A uint8 [T*k, H], A_e8m0 uint8 [T*k, H/32])."""
+    T, H = q.shape
+    R = T * k
+    A = np.zeros((R, H), dtype=np.uint8)
+    S = np.zeros((R, H // MX_BLOCK), dtype=np.uint8)
+    rows = np.asarray(pair_row, dtype=np.int64).reshape(T, k)
+    for j in range(k):
+        A[rows[:, j]] = q
+        S[rows[:, j]] = e8m0
+    return A, S
+
+
+def grouped_gemm1_mx(A, A_e8m0, Wq, W_e8m0, expert_offset, rows=None):
+    """Y[r, n] = bf16( sum_k deq(A)[r, k] * deq(W_e)[n, k] ) in fp64 for each
+    dense row r of expert e, with the MX scales (every product is exact)."""
+    R = A.shape[0]
+    rows = np.arange(R) if rows is None else np.asarray(rows, dtype=np.int64)
+    N = Wq.shape[1]
+    rexp = row_experts(expert_offset, R)[rows]
+    out = np.zeros((len(rows), N), dtype=np.uint16)
+    for e in np.unique(rexp):
+        sel = np.nonzero(rexp == e)[0]
+        a = dequantize_mx(A[rows[sel]], A_e8m0[rows[sel]])
+        w = dequantize_mx(Wq[e], W_e8m0[e])
+        out[sel] = f64_to_bf16(a @ w.T)
+    return out
