@@ -178,6 +178,10 @@ class Workload:
         self.Wq = torch.empty(E, N, H, dtype=torch.uint8, device=device)
         self.Ws = torch.empty(E, N // 128, H // 128, dtype=torch.float32, device=device)
         moe.moe_quant_weights(W, self.Wq, self.Ws)
+        # the MXFP8 variant's weights (e8m0 scales per 32 values), timed beside the fp32-scale path
+        self.Wq_mx = torch.empty(E, N, H, dtype=torch.uint8, device=device)
+        self.W_sf = torch.empty(moe.mx_sf_w_shape(E, N, H), dtype=torch.uint8, device=device)
+        moe.moe_quant_weights_mx(W, self.Wq_mx, self.W_sf)
         torch.cuda.synchronize(device)
         del W
         self.L = moe.Layout(T, k, E, G, device=device)
@@ -186,6 +190,8 @@ class Workload:
         self.Y = torch.empty(self.R, N, dtype=torch.bfloat16, device=device)
         self.out = torch.empty(T, N, dtype=torch.bfloat16, device=device)
         self.ws = torch.empty(int(self.L.sizes.stage1_ws_bytes), dtype=torch.uint8, device=device)
+        self.A_mx = torch.empty(self.R, H, dtype=torch.uint8, device=device)
+        self.A_sf = torch.empty(moe.mx_sf_a_shape(self.L, H), dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.opts = stage1_opts
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
@@ -221,6 +227,10 @@ class Workload:
     def dispatch_bytes(self):
         c = self.cfg
         return 2.0 * c.T * c.H + self.R * c.H + 4.0 * self.R * c.H / 128
+
+    def dispatch_bytes_mx(self):
+        c = self.cfg
+        return 2.0 * c.T * c.H + self.R * c.H + self.R * c.H / 32
 
     def combine_bytes(self):
         c = self.cfg
@@ -290,6 +300,9 @@ def run_gpu(args):
     u_disp = statistics.median(e[1].elapsed_time(e[4]) for e in uev)
     u_gemm = statistics.median(e[4].elapsed_time(e[2]) for e in uev)
 
+    # ---- the MXFP8 variant on the same step's layout: dispatch and block-scaled GEMM1
+    mx = run_mx_variant(wl, s, max(3, args.steps // 2))
+
     # ---- end to end through the public API with host buffers: H2D inputs, D2H output
     e2e = run_e2e(wl, s, args, world, device)
 
@@ -338,6 +351,9 @@ def run_gpu(args):
         "dispatch_gbs": round(wl.dispatch_bytes() / (u_disp / 1e3) / 1e9, 1),
         "combine_gbs": round(wl.combine_bytes() / (statistics.median(comb_ms) / 1e3) / 1e9, 1),
         "hbm_peak_gbs": peaks["hbm_gbs"],
+        "mx": dict(mx, gemm1_tflops=round(wl.gemm_flops() / (mx["gemm1_us"] / 1e6) / 1e12, 1),
+                   gemm1_frac_of_burst=round(wl.gemm_flops() / (mx["gemm1_us"] / 1e6) / 1e12 / fp8_burst, 4),
+                   dispatch_gbs=round(wl.dispatch_bytes_mx() / (mx["dispatch_us"] / 1e6) / 1e9, 1)),
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
@@ -350,6 +366,23 @@ def run_gpu(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_mx_variant(wl, s, reps):
+    """The MXFP8 variant (e8m0 scales per 32 values, block-scaled tcgen05 MMA)
+    on the step's layout: median CUDA-event times of its dispatch and its
+    GEMM1 over `reps` launches each, the L2 flushed before every launch."""
+    moe = wl.moe
+    moe.moe_route_layout(wl.ids, wl.w, wl.L, wl.status, stream=s)
+    d = _time_events(lambda: moe.moe_dispatch_quant_mx(wl.x, wl.L, wl.A_mx, wl.A_sf, wl.status, stream=s),
+                     s, reps, wl.flush)
+    g = _time_events(lambda: moe.moe_grouped_gemm1_mx(wl.A_mx, wl.A_sf, wl.Wq_mx, wl.W_sf, wl.L, wl.Y, wl.status,
+                                                       stream=s), s, reps, wl.flush)
+    torch.cuda.synchronize()
+    if wl.status.item() != 0:
+        raise RuntimeError(f"device status {moe.status_string(wl.status.item())} in the MX variant")
+    return {"dispatch_us": round(d, 1), "gemm1_us": round(g, 1),
+            "scales": "e8m0 per 32 values (amax/448 rounded up to a power of two), applied by the tensor core"}
 
 
 def run_e2e(wl, s, args, world, device):

@@ -27,6 +27,7 @@ EXPORTS = [
     "moe_status_string", "moe_layout_sizes", "moe_route_layout", "moe_dispatch_quant",
     "moe_grouped_gemm1", "moe_combine", "moe_stage1", "moe_router_topk", "moe_quant_weights",
     "moe_dequant_rows", "moe_device_sm_count", "moe_route_layout_noalloc",
+    "moe_dispatch_quant_mx", "moe_quant_weights_mx", "moe_grouped_gemm1_mx",
 ]
 
 
@@ -82,6 +83,9 @@ def lib() -> ctypes.CDLL:
         L.moe_dequant_rows.argtypes = [vp, vp, i32, ctypes.POINTER(LayoutC), vp, vp]
         L.moe_device_sm_count.argtypes = []
         L.moe_route_layout_noalloc.argtypes = [vp, vp, ctypes.POINTER(LayoutC), vp, vp]
+        L.moe_dispatch_quant_mx.argtypes = [vp, i32, ctypes.POINTER(LayoutC), vp, vp, vp, vp]
+        L.moe_quant_weights_mx.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        L.moe_grouped_gemm1_mx.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(LayoutC), vp, vp, vp]
         for n in EXPORTS:
             if n != "moe_status_string":
                 getattr(L, n).restype = i32
@@ -301,3 +305,53 @@ def moe_dequant_rows(A: torch.Tensor, A_scale: torch.Tensor, layout: Layout, Y: 
 
 def moe_device_sm_count() -> int:
     return int(lib().moe_device_sm_count())
+
+
+# ---------------------------------------------------------------- MXFP8 variant
+
+def mx_sf_a_shape(layout: Layout, H: int):
+    """Shape of the activation scale-factor buffer A_sf: [max_tiles, H/128, 512] bytes."""
+    return (layout.max_tiles, H // 128, 512)
+
+
+def mx_sf_w_shape(E: int, N: int, H: int):
+    """Shape of the weight scale-factor buffer W_sf: [E, H/128, N/128, 512] bytes."""
+    return (E, H // 128, N // 128, 512)
+
+
+def moe_dispatch_quant_mx(x: torch.Tensor, layout: Layout, A: torch.Tensor, A_sf: torch.Tensor,
+                          status: torch.Tensor, stream=None):
+    T, H = _dims(x, 2, "x")
+    R = layout.T * layout.k
+    _shape(x, (layout.T, H), "x")
+    _shape(A, (R, H), "A")
+    _shape(A_sf, mx_sf_a_shape(layout, H), "A_sf")
+    _status(status)
+    _check("moe_dispatch_quant_mx", lib().moe_dispatch_quant_mx(
+        _ptr(x, torch.bfloat16, "x"), H, ctypes.byref(layout.c), _ptr(A, torch.uint8, "A"),
+        _ptr(A_sf, torch.uint8, "A_sf"), _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def moe_quant_weights_mx(W: torch.Tensor, Wq: torch.Tensor, W_sf: torch.Tensor, stream=None):
+    E, N, H = _dims(W, 3, "W")
+    _shape(Wq, (E, N, H), "Wq")
+    _shape(W_sf, mx_sf_w_shape(E, N, H), "W_sf")
+    _check("moe_quant_weights_mx", lib().moe_quant_weights_mx(
+        _ptr(W, torch.bfloat16, "W"), E, N, H, _ptr(Wq, torch.uint8, "Wq"), _ptr(W_sf, torch.uint8, "W_sf"),
+        _stream(stream)))
+
+
+def moe_grouped_gemm1_mx(A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tensor, W_sf: torch.Tensor,
+                         layout: Layout, Y: torch.Tensor, status: torch.Tensor, stream=None):
+    E, N, H = _dims(W, 3, "W")
+    R = layout.T * layout.k
+    _shape(W, (layout.E, N, H), "W")
+    _shape(W_sf, mx_sf_w_shape(layout.E, N, H), "W_sf")
+    _shape(A, (R, H), "A")
+    _shape(A_sf, mx_sf_a_shape(layout, H), "A_sf")
+    _shape(Y, (R, N), "Y")
+    _status(status)
+    _check("moe_grouped_gemm1_mx", lib().moe_grouped_gemm1_mx(
+        _ptr(A, torch.uint8, "A"), _ptr(A_sf, torch.uint8, "A_sf"), _ptr(W, torch.uint8, "W"),
+        _ptr(W_sf, torch.uint8, "W_sf"), N, H, ctypes.byref(layout.c), _ptr(Y, torch.bfloat16, "Y"),
+        _ptr(status, torch.int32, "status"), _stream(stream)))

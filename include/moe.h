@@ -185,6 +185,48 @@ int moe_combine(const uint16_t* Y, int D, const moe_layout_t* L, uint16_t* out, 
                 moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * MXFP8 variant: e8m0 (power-of-two) scales per 32 values, applied by the
+ * tensor core's block-scaled MMA instead of in software ([mori] first commit:
+ * "GEMM1 reads its A rows and e8m0 scales through a rowmap"; quant-LDS commit:
+ * the e8m0 scales packed four per 32-bit word).  The pages give neither the
+ * block size nor the rule; this library takes 32 values per block (for the
+ * activations along H, for each weight row along K) and
+ *   X = the smallest integer with 448 * 2^X >= amax (amax / 448 rounded up to
+ *       a power of two), clamped to [-127, 127]; amax == 0 gives X = -127;
+ *   e8m0 code = X + 127; value code = e4m3(x * 2^-X) (round to nearest even,
+ *   saturating).
+ * Scale-factor layouts (MMA-ready; byte (i % 32) * 16 + (i / 32) * 4 + j of a
+ * 512-byte atom holds row i's code of 32-value chunk j of a 128-value K block):
+ *   A_sf  u8 [max_tiles][H/128][512]: atom of (M-tile m, K block kb); row i is
+ *         slot i of tile m (dense row tile_row_begin[m] + i).  Slots past the
+ *         tile's rows are never written (their content is ignored).
+ *   W_sf  u8 [E][H/128][N/128][512]: atom of (expert e, K block kb, weight
+ *         rows [128 nb, 128 nb + 128)).
+ * Buffers must be 16-byte aligned.  E <= 1024, H % 128 == 0, H <= 32768.
+ * ------------------------------------------------------------------------- */
+
+/* moe_dispatch_quant_mx: quantise each token once (MX rule above) and store
+ * it to each of its k rows: A as moe_dispatch_quant, scales into A_sf at the
+ * row's tile slot.  Rows of invalid pairs are not written. */
+int moe_dispatch_quant_mx(const uint16_t* x, int H, const moe_layout_t* L, uint8_t* A, uint8_t* A_sf,
+                          int32_t* status, moe_stream_t stream);
+
+/* moe_quant_weights_mx: expert weights bf16 [E, N, H] -> e4m3 codes [E, N, H]
+ * and W_sf (layout above), one scale per weight row and 32 values of K.
+ * N % 128 == 0, H % 128 == 0. */
+int moe_quant_weights_mx(const uint16_t* W, int E, int N, int H, uint8_t* Wq, uint8_t* W_sf,
+                         moe_stream_t stream);
+
+/* moe_grouped_gemm1_mx: Y[r, n] = bf16( sum_k (A[r,k] 2^XA[r,k/32]) (W[e,n,k] 2^XW[e,n,k/32]) )
+ * for every dense row r of expert e: one persistent tcgen05 kernel with
+ * kind::mxf8f6f4 block-scaled MMAs (M128 N256 K32), scales copied from A_sf /
+ * W_sf into tensor memory per K block, fp32 accumulation in tensor memory over
+ * the whole K, bf16 (round to nearest even) for the valid rows only.
+ * N % 256 == 0, H % 128 == 0, N, H <= 32768. */
+int moe_grouped_gemm1_mx(const uint8_t* A, const uint8_t* A_sf, const uint8_t* W, const uint8_t* W_sf, int N,
+                         int H, const moe_layout_t* L, uint16_t* Y, int32_t* status, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Fused stage1 ([tilepipe] "Overlap": SMs partitioned between a producer that
  * bumps a semaphore per finished tile and a consumer GEMM waiting on it,
  * producer order chosen to unblock the expert-major GEMM order as early as

@@ -64,3 +64,38 @@ def compare_layout(L: moe.Layout, ref: dict):
             assert np.array_equal(g.view(np.uint32), np.asarray(want, np.float32).view(np.uint32)), name
         else:
             assert np.array_equal(g, np.asarray(want)), f"{name} differs"
+
+
+# ---------------------------------------------------------------- MX scale-factor layouts
+# The MX variant stores its e8m0 codes in 512-byte atoms: byte
+# (i % 32) * 16 + (i // 32) * 4 + j of an atom holds row i's code of 32-value
+# chunk j of one 128-value K block (the layout stated in include/moe.h).  These
+# read the codes back per row, so they compare with the oracle's [rows, H/32].
+
+def _atom_byte(i):
+    i = np.asarray(i, dtype=np.int64)
+    return (i % 32) * 16 + (i // 32) * 4
+
+
+def sf_a_rows(A_sf: np.ndarray, ref: dict, rows: np.ndarray) -> np.ndarray:
+    """A_sf [max_tiles, H/128, 512] -> e8m0 codes [len(rows), H/32] of dense rows
+    ``rows``, placed by the oracle layout's tile of each row."""
+    rows = np.asarray(rows, dtype=np.int64)
+    eo = np.asarray(ref["expert_offset"], np.int64)
+    eto = np.asarray(ref["expert_tile_offset"], np.int64)
+    e = np.searchsorted(eo, rows, side="right") - 1
+    rel = rows - eo[e]
+    m, i = eto[e] + rel // 128, rel % 128
+    KB = A_sf.shape[1]
+    idx = _atom_byte(i)[:, None, None] + np.arange(4)[None, None, :]              # [n, 1, 4]
+    out = A_sf[m[:, None, None], np.arange(KB)[None, :, None], idx]                 # [n, KB, 4]
+    return out.reshape(len(rows), KB * 4)
+
+
+def sf_w_rows(W_sf: np.ndarray, e: int, n_rows: np.ndarray) -> np.ndarray:
+    """W_sf [E, H/128, N/128, 512] -> e8m0 codes [len(n_rows), H/32] of expert e's rows."""
+    n_rows = np.asarray(n_rows, dtype=np.int64)
+    KB = W_sf.shape[1]
+    idx = _atom_byte(n_rows % 128)[:, None, None] + np.arange(4)[None, None, :]
+    out = W_sf[e][np.arange(KB)[None, :, None], (n_rows // 128)[:, None, None], idx]
+    return out.reshape(len(n_rows), KB * 4)

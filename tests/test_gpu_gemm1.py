@@ -51,7 +51,7 @@ def oracle_rows_expected(cfg, W, ids, w, rows):
     R = cfg.T * cfg.k
     rexp = oracle.row_experts(ref["expert_offset"], R)[rows]
     toks = ref["row_pair"][rows].astype(np.int64) // cfg.k
-    q, s = oracle.quantize_rows(inputs.bf16_bits(inputs.make_x(cfg.T, cfg.H, cfg.seed)[toks]))
+    q, s = oracle.quantize_rows(inputs.bf16_bits(inputs.make_x(cfg.T, cfg.H, cfg.seed)[torch.as_tensor(toks)]))
     want = np.zeros((len(rows), cfg.N), np.uint16)
     wq = {}
     for e in np.unique(rexp):
