@@ -664,7 +664,8 @@ def run_bw_sweep(args):
 
 def run_layout_sweep(args):
     """Routing layout call latency vs batch (E=256, k=8, Zipf 1.2 routing): one
-    block in a plain launch up to T = 32, the cooperative grid above."""
+    block in a plain launch up to T = 32, the cooperative grid above; the
+    no-plan layout beside it up to T*k = 16384 pairs."""
     import combine_counting_sort_gb300 as moe
     from combine_counting_sort_gb300 import inputs
     import __graft_entry__ as ge
@@ -673,7 +674,7 @@ def run_layout_sweep(args):
     s = torch.cuda.Stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     E, G, k = 256, 8, 8
-    for T in (8, 32, 33, 128, 512, 2048, 8192, 16384):
+    for T in (8, 32, 33, 128, 256, 512, 1024, 2048, 8192, 16384):
         logits = inputs.make_logits(T, E, 1.2, 0).to(dev)
         ids = torch.empty(T, k, dtype=torch.int32, device=dev)
         w = torch.empty(T, k, dtype=torch.float32, device=dev)
@@ -681,10 +682,15 @@ def run_layout_sweep(args):
         L = moe.Layout(T, k, E, G, device=dev)
         st = torch.zeros(1, dtype=torch.int32, device=dev)
         us = _time_events(lambda: moe.moe_route_layout(ids, w, L, st, stream=s), s, args.steps, flush)
+        line = {"sweep": "layout", "T": T, "k": k, "E": E, "pairs": T * k, "layout_us": round(us, 1),
+                "blocks": "one (plain launch)" if T <= 32 else "grid (cooperative)"}
+        if T * k <= moe.MOE_NOPLAN_MAX_PAIRS:
+            # the no-plan layout: reservation atomics in one block, rows in reservation order
+            line["noplan_us"] = round(_time_events(lambda: moe.moe_route_layout_noplan(ids, w, L, st, stream=s),
+                                                   s, args.steps, flush), 1)
         torch.cuda.synchronize()
         assert st.item() == 0
-        print(json.dumps({"sweep": "layout", "T": T, "k": k, "E": E, "pairs": T * k, "layout_us": round(us, 1),
-                          "blocks": "one (plain launch)" if T <= 32 else "grid (cooperative)"}), flush=True)
+        print(json.dumps(line), flush=True)
 
 
 def run_stage1_sweep(args):

@@ -27,7 +27,7 @@ EXPORTS = [
     "moe_status_string", "moe_layout_sizes", "moe_route_layout", "moe_dispatch_quant",
     "moe_grouped_gemm1", "moe_combine", "moe_stage1", "moe_router_topk", "moe_quant_weights",
     "moe_dequant_rows", "moe_device_sm_count", "moe_route_layout_noalloc",
-    "moe_dispatch_quant_mx", "moe_quant_weights_mx", "moe_grouped_gemm1_mx",
+    "moe_dispatch_quant_mx", "moe_quant_weights_mx", "moe_grouped_gemm1_mx", "moe_route_layout_noplan",
 ]
 
 
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
         L.moe_dequant_rows.argtypes = [vp, vp, i32, ctypes.POINTER(LayoutC), vp, vp]
         L.moe_device_sm_count.argtypes = []
         L.moe_route_layout_noalloc.argtypes = [vp, vp, ctypes.POINTER(LayoutC), vp, vp]
+        L.moe_route_layout_noplan.argtypes = [vp, vp, ctypes.POINTER(LayoutC), vp, vp]
         L.moe_dispatch_quant_mx.argtypes = [vp, i32, ctypes.POINTER(LayoutC), vp, vp, vp, vp]
         L.moe_quant_weights_mx.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.moe_grouped_gemm1_mx.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(LayoutC), vp, vp, vp]
@@ -192,6 +193,22 @@ def moe_route_layout_noalloc(topk_ids: torch.Tensor, topk_w: torch.Tensor, layou
     _shape(topk_w, (layout.T, layout.k), "topk_w")
     _status(status)
     _check("moe_route_layout_noalloc", lib().moe_route_layout_noalloc(
+        _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(topk_w, torch.float32, "topk_w"), ctypes.byref(layout.c),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+MOE_NOPLAN_MAX_PAIRS = 16384
+
+
+def moe_route_layout_noplan(topk_ids: torch.Tensor, topk_w: torch.Tensor, layout: Layout, status: torch.Tensor,
+                            stream=None):
+    """The small-batch layout without the counting sort (T*k <= 16384): the
+    same tables as moe_route_layout except that rows within an expert (and
+    tokens within a first-expert group) come in reservation order."""
+    _shape(topk_ids, (layout.T, layout.k), "topk_ids")
+    _shape(topk_w, (layout.T, layout.k), "topk_w")
+    _status(status)
+    _check("moe_route_layout_noplan", lib().moe_route_layout_noplan(
         _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(topk_w, torch.float32, "topk_w"), ctypes.byref(layout.c),
         _ptr(status, torch.int32, "status"), _stream(stream)))
 

@@ -591,3 +591,166 @@ extern "C" int moe_route_layout_noalloc(const int32_t* topk_ids, const float* to
   if (rc) return rc;
   return launch_layout(topk_ids, topk_w, L, ws, status, (cudaStream_t)stream);
 }
+
+// ---------------------------------------------------------------- no-plan layout (small batches)
+//
+// The mori stage1 page's --no-plan ("How it works now"): no counting sort --
+// one reservation atomic per worker and run, no histogram pass, no prefix sum
+// over the batch, no grid rendezvous -- worth it while a batch is small
+// ("What each mechanism is worth": -12 us at 256 tokens, -5 at 512, +23 at
+// 1024).  Here: ONE block of 1024 threads.  Each warp reserves, per expert
+// its 32 pairs route to, one run of consecutive slots with a single
+// shared-memory atomic (lanes with equal experts find each other with
+// __match_any_sync and take consecutive slots of the run), and the same for
+// each token's first expert; one block scan over the E counts then gives the
+// expert offsets and the tile tables, and every pair lands at its expert's
+// offset plus its slot.  The tables are the counting sort's except for the
+// order of the rows within an expert (and of the tokens within a
+// first-expert group), which follows the atomics: as a multiset per expert
+// they are the same.  No workspace, nothing to zero between calls.
+
+namespace moe {
+constexpr int kNoPlanThreads = 1024;
+constexpr int kNoPlanPer = MOE_NOPLAN_MAX_PAIRS / kNoPlanThreads;   // pairs (and tokens) per thread
+
+// Warp-aggregated reservation: every lane whose key is >= 0 gets a distinct
+// slot of counter[key]; lanes with equal keys take consecutive slots, one
+// atomic per key per warp.  Whole warp, converged.
+__device__ __forceinline__ int reserve_slot(int* counter, int key) {
+  const int lane = threadIdx.x & 31;
+  const unsigned peers = __match_any_sync(0xffffffffu, key);
+  const int leader = __ffs(peers) - 1;
+  int base = 0;
+  if (key >= 0 && lane == leader) base = atomicAdd(&counter[key], __popc(peers));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return key >= 0 ? base + __popc(peers & lanemask_lt()) : -1;
+}
+
+__global__ void __launch_bounds__(kNoPlanThreads, 1)
+    route_layout_noplan_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, LayoutDev L,
+                               int32_t* status) {
+  extern __shared__ int smem_np[];
+  const int E = L.E, k = L.k, T = L.T, BM = L.block_m;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = T * k;
+  int* cnt = smem_np;          // [E]   pairs per expert (the reservation counters)
+  int* fcnt = cnt + E;         // [E]   tokens per first expert
+  int* eoff = fcnt + E;        // [E+1] expert offsets
+  int* toff = eoff + E + 1;    // [E+1] expert tile offsets
+  int* foff = toff + E + 1;    // [E+1] first-expert offsets
+  int* scratch = foff + E + 1; // [64]
+  int* s_ids = scratch + 64;   // [P]   the batch's expert ids, staged once
+  float* s_w = reinterpret_cast<float*>(s_ids + P);   // [P]
+  for (int e = tid; e < E; e += blockDim.x) { cnt[e] = 0; fcnt[e] = 0; }
+  // one coalesced pass over the inputs: every later read comes from shared memory
+  for (int p = tid; p < P; p += blockDim.x) {
+    s_ids[p] = __ldcs(ids + p);
+    s_w[p] = __ldcs(w + p);
+  }
+  __syncthreads();
+
+  const int rounds = (max(P, T) + kNoPlanThreads - 1) / kNoPlanThreads;   // block-uniform
+  // (key << 16) | slot per pair and per token (-1: none); keys < 1024, slots < 2^15
+  int pk[kNoPlanPer], tk[kNoPlanPer];
+#pragma unroll
+  for (int i = 0; i < kNoPlanPer; ++i) {
+    pk[i] = -1;
+    tk[i] = -1;
+    if (i < rounds) {
+      const int p = tid + i * kNoPlanThreads;
+      int e = -1;
+      if (p < P) {
+        e = s_ids[p];
+        if (e < 0 || e >= E) { set_status(status, MOE_ERR_EXPERT_ID); e = -1; }
+      }
+      const int ps = reserve_slot(cnt, e);
+      if (e >= 0) pk[i] = (e << 16) | ps;
+      const int t = tid + i * kNoPlanThreads;
+      int fe = -1;
+      if (t < T) {
+        fe = first_expert(s_ids + (size_t)t * k, k, E);
+        if (fe >= E) fe = -1;
+      }
+      const int ts = reserve_slot(fcnt, fe);
+      if (fe >= 0) tk[i] = (fe << 16) | ts;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    eoff[e] = cnt[e];
+    toff[e] = (cnt[e] + BM - 1) / BM;
+    foff[e] = fcnt[e];
+  }
+  __syncthreads();
+  const int total_rows = block_exclusive_scan(eoff, E, scratch);
+  const int total_tiles = block_exclusive_scan(toff, E, scratch);
+  const int total_first = block_exclusive_scan(foff, E, scratch);
+  if (tid == 0) { eoff[E] = total_rows; toff[E] = total_tiles; foff[E] = total_first; }
+  __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) {
+    if (e < E) {
+      L.count[e] = cnt[e];
+      L.ready_tokens[e] = foff[e + 1];
+    }
+    L.expert_offset[e] = eoff[e];
+    L.expert_tile_offset[e] = toff[e];
+  }
+  const int epg = E / L.G;
+  for (int g = tid; g <= L.G; g += blockDim.x) L.group_offset[g] = eoff[g * epg];
+  if (tid == 0) L.num_tiles[0] = total_tiles;
+  // every pair to its expert's offset plus its slot; every token after its first expert's offset
+#pragma unroll
+  for (int i = 0; i < kNoPlanPer; ++i) {
+    if (i < rounds) {
+      const int p = tid + i * kNoPlanThreads;
+      if (p < P) {
+        if (pk[i] >= 0) {
+          const int row = eoff[pk[i] >> 16] + (pk[i] & 0xFFFF);
+          L.pair_row[p] = row;
+          L.row_pair[row] = p;
+          L.row_weight[row] = s_w[p];
+        } else {
+          L.pair_row[p] = -1;
+        }
+      }
+      const int t = tid + i * kNoPlanThreads;
+      if (tk[i] >= 0) L.token_order[foff[tk[i] >> 16] + (tk[i] & 0xFFFF)] = t;
+    }
+  }
+  // tile tables and rowmap, one warp per tile (as the counting-sort layout)
+  for (int m = warp; m < L.max_tiles; m += kNoPlanThreads / 32) {
+    int e = -1, begin = T * k, rows = 0;
+    if (m < total_tiles) {
+      int lo = 0, hi = E;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (toff[mid] <= m) lo = mid; else hi = mid;
+      }
+      e = lo;
+      begin = eoff[e] + (m - toff[e]) * BM;
+      rows = min(BM, eoff[e + 1] - begin);
+    }
+    if (lane == 0) {
+      L.tile_expert[m] = e;
+      L.tile_row_begin[m] = begin;
+      L.tile_rows[m] = rows;
+    }
+    int32_t* slot = L.rowmap + (size_t)m * BM;
+    for (int j = lane; j < BM; j += 32) slot[j] = j < rows ? begin + j : -1;
+  }
+}
+}  // namespace moe
+
+extern "C" int moe_route_layout_noplan(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
+                                       int32_t* status, moe_stream_t stream) {
+  int rc = check_layout(L);
+  if (rc) return rc;
+  if (!topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if ((long long)L->T * L->k > MOE_NOPLAN_MAX_PAIRS) return MOE_ERR_UNSUPPORTED;
+  const size_t smem = sizeof(int) * (size_t)(2 * L->E + 3 * (L->E + 1) + 64 + 2 * (size_t)L->T * L->k);
+  if (cudaFuncSetAttribute(route_layout_noplan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  route_layout_noplan_kernel<<<1, kNoPlanThreads, smem, (cudaStream_t)stream>>>(topk_ids, topk_w, to_dev(L), status);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

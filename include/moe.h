@@ -148,6 +148,25 @@ int moe_route_layout(const int32_t* topk_ids, const float* topk_w, const moe_lay
 int moe_route_layout_noalloc(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
                              int32_t* status, moe_stream_t stream);
 
+/* moe_route_layout_noplan: the layout without the counting sort, for small
+ * batches ([mori] "How it works now", --no-plan: one reservation atomic per
+ * worker and run, no histogram, no prefix sum over the batch, no grid
+ * rendezvous; "What each mechanism is worth": a gain at 256 and 512 tokens, a
+ * loss at 1024).  One block: each warp reserves one run of consecutive slots
+ * per expert its pairs route to with a single shared-memory atomic, then one
+ * scan over the E counts places the runs.  Every table equals
+ * moe_route_layout's EXCEPT the order of the rows within an expert
+ * (pair_row, row_pair, row_weight) and of the tokens within a first-expert
+ * group (token_order): those follow the atomics and change from call to call;
+ * as a multiset per expert (per first expert) they are the same.  Counts,
+ * offsets, tile tables, rowmap, group offsets and ready_tokens are identical.
+ *   Limit: T * k <= MOE_NOPLAN_MAX_PAIRS (larger returns MOE_ERR_UNSUPPORTED).
+ *   No workspace: everything lives in the block's shared memory.  Invalid
+ *   ids as moe_route_layout. */
+#define MOE_NOPLAN_MAX_PAIRS 16384
+int moe_route_layout_noplan(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
+                            int32_t* status, moe_stream_t stream);
+
 /* moe_dispatch_quant: quantise each token once and store it to each of its k
  * rows ([mori] "How it works now" and the quant-once commit: read and quantise
  * a token once, store it to every run it is in).  Per token t and block b of
