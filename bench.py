@@ -190,6 +190,7 @@ class Workload:
         self.Y = torch.empty(self.R, N, dtype=torch.bfloat16, device=device)
         self.out = torch.empty(T, N, dtype=torch.bfloat16, device=device)
         self.ws = torch.empty(int(self.L.sizes.stage1_ws_bytes), dtype=torch.uint8, device=device)
+        self.ws_gc = torch.empty(int(self.L.sizes.gemm_combine_ws_bytes), dtype=torch.uint8, device=device)
         self.A_mx = torch.empty(self.R, H, dtype=torch.uint8, device=device)
         self.A_sf = torch.empty(moe.mx_sf_a_shape(self.L, H), dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
@@ -197,24 +198,36 @@ class Workload:
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
         torch.cuda.empty_cache()
 
-    def step(self, s, ev=None, fused=True, ids=None, w=None):
-        """One pass of the hot path on stream s; ev = 4 events (layout | stage1 | combine)."""
+    def calls(self, s, variant, ids=None, w=None):
+        """The step's calls in order, as (part name, thunk) pairs, on stream s:
+        fused    layout | stage1 (one launch: quant + dispatch + GEMM1) | combine
+        unfused  layout | dispatch | GEMM1 | combine
+        overlap  layout | dispatch | GEMM1 with the combine overlapped (one launch)"""
         moe = self.moe
         ids = self.ids if ids is None else ids
         w = self.w if w is None else w
-        if ev: ev[0].record(s)
-        moe.moe_route_layout(ids, w, self.L, self.status, stream=s)
-        if ev: ev[1].record(s)
-        if fused:
-            moe.moe_stage1(self.x, self.L, self.Wq, self.Ws, self.A, self.As, self.Y, self.ws, self.status,
-                           self.opts, stream=s)
-        else:
-            moe.moe_dispatch_quant(self.x, self.L, self.A, self.As, self.status, stream=s)
-            if ev and len(ev) > 4: ev[4].record(s)
-            moe.moe_grouped_gemm1(self.A, self.As, self.Wq, self.Ws, self.L, self.Y, self.status, stream=s)
-        if ev: ev[2].record(s)
-        moe.moe_combine(self.Y, self.L, self.out, self.status, stream=s)
-        if ev: ev[3].record(s)
+        layout = ("layout", lambda: moe.moe_route_layout(ids, w, self.L, self.status, stream=s))
+        dispatch = ("dispatch", lambda: moe.moe_dispatch_quant(self.x, self.L, self.A, self.As, self.status, stream=s))
+        gemm1 = ("gemm1", lambda: moe.moe_grouped_gemm1(self.A, self.As, self.Wq, self.Ws, self.L, self.Y, self.status,
+                                                        stream=s))
+        combine = ("combine", lambda: moe.moe_combine(self.Y, self.L, self.out, self.status, stream=s))
+        if variant == "fused":
+            return [layout, ("stage1", lambda: moe.moe_stage1(self.x, self.L, self.Wq, self.Ws, self.A, self.As, self.Y,
+                                                              self.ws, self.status, self.opts, stream=s)), combine]
+        if variant == "unfused":
+            return [layout, dispatch, gemm1, combine]
+        if variant == "overlap":
+            return [layout, dispatch, ("gemm1_combine", lambda: moe.moe_grouped_gemm1_combine(
+                self.A, self.As, self.Wq, self.Ws, self.L, self.Y, self.out, self.ws_gc, self.status, stream=s))]
+        raise ValueError(variant)
+
+    def step(self, s, variant, ev=None, ids=None, w=None):
+        """One pass of the hot path on stream s; ev: one event before each call and one after the last."""
+        calls = self.calls(s, variant, ids, w)
+        for i, (_, fn) in enumerate(calls):
+            if ev: ev[i].record(s)
+            fn()
+        if ev: ev[len(calls)].record(s)
 
     def flush_l2(self, s):
         with torch.cuda.stream(s):
@@ -237,15 +250,25 @@ class Workload:
         return 2.0 * self.R * c.N + 2.0 * c.T * c.N + 8.0 * self.R
 
 
-def timed_loop(wl, s, steps, fused, n_ev):
+VARIANTS = ["fused", "unfused", "overlap"]
+ROOFLINE_PART = {"fused": ("stage1", "stage1_kernel"), "unfused": ("gemm1", "grouped_gemm1_kernel"),
+                 "overlap": ("gemm1_combine", "grouped_gemm1_combine_kernel")}
+
+
+def timed_loop(wl, s, steps, variant):
+    """`steps` steps of `variant`, the L2 flushed before each (outside the events).
+    Returns (per-step ms, {part: [ms per step]})."""
+    names = [n for n, _ in wl.calls(s, variant)]
     evs = []
     for _ in range(steps):
         wl.flush_l2(s)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-        wl.step(s, ev, fused=fused)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+        wl.step(s, variant, ev)
         evs.append(ev)
     torch.cuda.synchronize()
-    return evs
+    step_ms = [e[0].elapsed_time(e[-1]) for e in evs]
+    parts = {n: [e[i].elapsed_time(e[i + 1]) for e in evs] for i, n in enumerate(names)}
+    return step_ms, parts
 
 
 def run_gpu(args):
@@ -265,11 +288,12 @@ def run_gpu(args):
                            producers_join=args.join)
     wl = Workload(cfg, device, opts)
     s = torch.cuda.Stream(device)
-    fused = args.variant == "fused"
+    variant = args.variant
 
-    for _ in range(args.warmup):
-        wl.flush_l2(s)
-        wl.step(s, fused=fused)
+    for v in VARIANTS:            # every variant warmed up (each is timed below)
+        for _ in range(args.warmup):
+            wl.flush_l2(s)
+            wl.step(s, v)
     torch.cuda.synchronize()
     if wl.status.item() != 0:
         raise RuntimeError(f"device status {moe.status_string(wl.status.item())} after warm-up")
@@ -279,26 +303,35 @@ def run_gpu(args):
     torch.cuda.synchronize()
     clocks = ClockSampler(local, enabled=not args.no_clocks)
     t_wall = time.perf_counter()
-    evs = timed_loop(wl, s, args.steps, fused, 4)
+    step_ms, parts = timed_loop(wl, s, args.steps, variant)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     barrier(world)
     clk = clocks.stop()
     if wl.status.item() != 0:
         raise RuntimeError(f"device status {moe.status_string(wl.status.item())} in the timed region")
-
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    layout_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    stage_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
     total_ms = reduce_max(sum(step_ms), world, device)
     ms_per_step = total_ms / args.steps
     value = world * cfg.T / (ms_per_step / 1e3)
 
-    # ---- the unfused chain of the same step, for the fused-vs-sum comparison
-    uev = timed_loop(wl, s, max(3, args.steps // 2), False, 5)
-    u_disp = statistics.median(e[1].elapsed_time(e[4]) for e in uev)
-    u_gemm = statistics.median(e[4].elapsed_time(e[2]) for e in uev)
+    # ---- the other step variants on the same inputs, for comparison (not part of `value`)
+    med = lambda xs: statistics.median(xs)
+    variants = {variant: {"ms_per_step": round(statistics.mean(step_ms), 4),
+                          "parts_us": {n: round(med(v) * 1e3, 1) for n, v in parts.items()}}}
+    vparts = {variant: parts}
+    for v in VARIANTS:
+        if v == variant:
+            continue
+        sm, pt = timed_loop(wl, s, max(3, args.steps // 2), v)
+        variants[v] = {"ms_per_step": round(statistics.mean(sm), 4),
+                       "parts_us": {n: round(med(x) * 1e3, 1) for n, x in pt.items()}}
+        vparts[v] = pt
+    if wl.status.item() != 0:
+        raise RuntimeError(f"device status {moe.status_string(wl.status.item())} in the variant runs")
+    u = vparts["unfused"]
+    u_disp, u_gemm, u_comb = med(u["dispatch"]), med(u["gemm1"]), med(u["combine"])
+    st1 = med(vparts["fused"]["stage1"])
+    gc = med(vparts["overlap"]["gemm1_combine"])
 
     # ---- the MXFP8 variant on the same step's layout: dispatch and block-scaled GEMM1
     mx = run_mx_variant(wl, s, max(3, args.steps // 2))
@@ -311,27 +344,31 @@ def run_gpu(args):
     fp8_sustained = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
     peak_kind = roofline_peak_kind(t_wall, clk)
     fp8_peak = fp8_sustained if peak_kind == "sustained" else fp8_burst
-    stage_avg = statistics.mean(stage_ms) if fused else u_gemm
-    variant_key = "%s/comm%d/%s/%s/join%d" % (args.variant, args.comm_sms, ["per_tile", "per_expert"][args.flags],
-                                              ["expert_major", "ready_first"][args.schedule], args.join)
+    part, kernel = ROOFLINE_PART[variant]
+    roof_ms = statistics.mean(parts[part])
+    variant_key = variant if variant != "fused" else "fused/comm%d/%s/%s/join%d" % (
+        args.comm_sms, ["per_tile", "per_expert"][args.flags], ["expert_major", "ready_first"][args.schedule],
+        args.join)
     traffic = args.traffic if args.traffic is not None else \
         TRAFFIC.get((cfg.name, variant_key, kernel_source_hash()))
-    achieved = wl.gemm_flops() / (stage_avg / 1e3) / 1e12
+    achieved = wl.gemm_flops() / (roof_ms / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate, bf16 out)",
         "data": "synthetic (seeded: x~N(0,1) bf16, logits~N(0,1)+Zipf bias, W1~N(0,1/H) quantised on device)",
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "G": cfg.G, "k": cfg.k, "N": cfg.N,
-                   "zipf": cfg.zipf, "step": "route_layout + stage1 (%s) + combine" % args.variant,
+                   "zipf": cfg.zipf, "variant": variant,
+                   "step": " | ".join(n for n, _ in wl.calls(s, variant)),
                    "stage1_opts": {"comm_sms": args.comm_sms, "flags": ["per_tile", "per_expert"][args.flags],
                                    "schedule": ["expert_major", "ready_first"][args.schedule],
                                    "producers_join": args.join},
                    "l2": "flushed between steps (512 MiB write, outside the step events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "stage1_kernel" if fused else "grouped_gemm1_kernel", "bound": "tensor",
+        "roofline": {"kernel": kernel, "bound": "tensor",
                      "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / fp8_peak, 4),
+                     "work": "2*T*k*N*H GEMM1 flops (valid rows) / mean duration of the %s call" % part,
                      "peak_kind": peak_kind,
                      "peak_source": f"{peaks['source']} bf16 {peak_kind} x {FP8_OVER_BF16} (fp8/bf16 nominal); "
                                     + PEAK_RULE,
@@ -341,21 +378,25 @@ def run_gpu(args):
                      "traffic": traffic,
                      "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one full-size launch"
                      if traffic is not None else None},
-        "stage1_us": round(statistics.median(stage_ms) * 1e3, 1),
-        "layout_us": round(statistics.median(layout_ms) * 1e3, 1),
-        "combine_us": round(statistics.median(comb_ms) * 1e3, 1),
+        "parts_us": variants[variant]["parts_us"],
+        "variants": variants,
+        "layout_us": round(med(parts["layout"]) * 1e3, 1),
+        "stage1_us": round(st1 * 1e3, 1),
         "unfused_us": {"dispatch": round(u_disp * 1e3, 1), "gemm1": round(u_gemm * 1e3, 1),
                        "sum": round((u_disp + u_gemm) * 1e3, 1)},
+        "combine_us": round(u_comb * 1e3, 1),
+        "gemm1_combine_us": round(gc * 1e3, 1),
+        "gemm1_plus_combine_us": round((u_gemm + u_comb) * 1e3, 1),
         "gemm1_tflops": round(wl.gemm_flops() / (u_gemm / 1e3) / 1e12, 1),
-        "stage1_tflops": round(wl.gemm_flops() / (statistics.median(stage_ms) / 1e3) / 1e12, 1),
+        "stage1_tflops": round(wl.gemm_flops() / (st1 / 1e3) / 1e12, 1),
         "dispatch_gbs": round(wl.dispatch_bytes() / (u_disp / 1e3) / 1e9, 1),
-        "combine_gbs": round(wl.combine_bytes() / (statistics.median(comb_ms) / 1e3) / 1e9, 1),
+        "combine_gbs": round(wl.combine_bytes() / (u_comb / 1e3) / 1e9, 1),
         "hbm_peak_gbs": peaks["hbm_gbs"],
         "mx": dict(mx, gemm1_tflops=round(wl.gemm_flops() / (mx["gemm1_us"] / 1e6) / 1e12, 1),
                    gemm1_frac_of_burst=round(wl.gemm_flops() / (mx["gemm1_us"] / 1e6) / 1e12 / fp8_burst, 4),
                    dispatch_gbs=round(wl.dispatch_bytes_mx() / (mx["dispatch_us"] / 1e6) / 1e9, 1)),
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": len(parts) * args.steps,
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 3),
     }
@@ -395,7 +436,6 @@ def run_e2e(wl, s, args, world, device):
     before the first H2D to one after the last D2H.  No L2 flush: a step's
     working set (weights of the used experts, x, A, Y) is ~6 GB, far above L2."""
     T, H, k, N = wl.cfg.T, wl.cfg.H, wl.cfg.k, wl.cfg.N
-    fused = args.variant == "fused"
     hx = [wl.x.cpu().pin_memory() for _ in range(2)]
     hids = [wl.ids.cpu().pin_memory() for _ in range(2)]
     hw = [wl.w.cpu().pin_memory() for _ in range(2)]
@@ -435,7 +475,7 @@ def run_e2e(wl, s, args, world, device):
             if i >= 2:
                 s.wait_event(out_done[i - 2])         # out[b] of step i-2 is on the host
             wl.x, wl.out = dx[b], dout[b]
-            wl.step(s, fused=fused, ids=dids[b], w=dw[b])
+            wl.step(s, args.variant, ids=dids[b], w=dw[b])
             comp_done[i].record(s)
             c_out.wait_event(comp_done[i])
             with torch.cuda.stream(c_out):
@@ -734,7 +774,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="t8192_zipf1.2")
-    ap.add_argument("--variant", choices=["fused", "unfused"], default="fused")
+    ap.add_argument("--variant", choices=VARIANTS, default="overlap",
+                    help="the step timed for `value`; the others are timed beside it")
     ap.add_argument("--comm-sms", type=int, default=36)
     ap.add_argument("--flags", type=int, default=0, help="0 per-tile, 1 per-expert")
     ap.add_argument("--schedule", type=int, default=0, help="0 expert-major, 1 ready-first")

@@ -28,6 +28,7 @@ EXPORTS = [
     "moe_grouped_gemm1", "moe_combine", "moe_stage1", "moe_router_topk", "moe_quant_weights",
     "moe_dequant_rows", "moe_device_sm_count", "moe_route_layout_noalloc",
     "moe_dispatch_quant_mx", "moe_quant_weights_mx", "moe_grouped_gemm1_mx", "moe_route_layout_noplan",
+    "moe_grouped_gemm1_combine",
 ]
 
 
@@ -39,7 +40,8 @@ class MoEError(RuntimeError):
 
 class LayoutSizes(ctypes.Structure):
     _fields_ = [("pairs", ctypes.c_int64), ("max_tiles", ctypes.c_int64), ("rowmap_len", ctypes.c_int64),
-                ("layout_ws_bytes", ctypes.c_size_t), ("stage1_ws_bytes", ctypes.c_size_t)]
+                ("layout_ws_bytes", ctypes.c_size_t), ("stage1_ws_bytes", ctypes.c_size_t),
+                ("gemm_combine_ws_bytes", ctypes.c_size_t)]
 
 
 _TABLES = ["count", "expert_offset", "expert_tile_offset", "group_offset", "ready_tokens", "pair_row",
@@ -83,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.moe_dequant_rows.argtypes = [vp, vp, i32, ctypes.POINTER(LayoutC), vp, vp]
         L.moe_device_sm_count.argtypes = []
         L.moe_route_layout_noalloc.argtypes = [vp, vp, ctypes.POINTER(LayoutC), vp, vp]
+        L.moe_grouped_gemm1_combine.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(LayoutC), vp, vp, vp, sz,
+                                                vp, vp]
         L.moe_route_layout_noplan.argtypes = [vp, vp, ctypes.POINTER(LayoutC), vp, vp]
         L.moe_dispatch_quant_mx.argtypes = [vp, i32, ctypes.POINTER(LayoutC), vp, vp, vp, vp]
         L.moe_quant_weights_mx.argtypes = [vp, i32, i32, i32, vp, vp, vp]
@@ -240,6 +244,37 @@ def moe_grouped_gemm1(A: torch.Tensor, A_scale: torch.Tensor, W: torch.Tensor, W
         _ptr(A, torch.uint8, "A"), _ptr(A_scale, torch.float32, "A_scale"), _ptr(W, torch.uint8, "W"),
         _ptr(W_scale, torch.float32, "W_scale"), N, H, ctypes.byref(layout.c), _ptr(Y, torch.bfloat16, "Y"),
         _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def moe_grouped_gemm1_combine(A: torch.Tensor, A_scale: torch.Tensor, W: torch.Tensor, W_scale: torch.Tensor,
+                              layout: Layout, Y: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                              status: torch.Tensor, stream=None):
+    """GEMM1 and the combine in one launch, each token combined once its k
+    expert outputs are stored (ws: layout.sizes.gemm_combine_ws_bytes bytes)."""
+    E, N, H = _dims(W, 3, "W")
+    R = layout.T * layout.k
+    _shape(W, (layout.E, N, H), "W")
+    _shape(W_scale, (layout.E, N // 128, H // 128), "W_scale")
+    _shape(A, (R, H), "A")
+    _shape(A_scale, (H // 128, R), "A_scale")
+    _shape(Y, (R, N), "Y")
+    _shape(out, (layout.T, N), "out")
+    _status(status)
+    _check("moe_grouped_gemm1_combine", lib().moe_grouped_gemm1_combine(
+        _ptr(A, torch.uint8, "A"), _ptr(A_scale, torch.float32, "A_scale"), _ptr(W, torch.uint8, "W"),
+        _ptr(W_scale, torch.float32, "W_scale"), N, H, ctypes.byref(layout.c), _ptr(Y, torch.bfloat16, "Y"),
+        _ptr(out, torch.bfloat16, "out"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def gemm_combine_trace(ws: torch.Tensor) -> dict:
+    """Trace of the last moe_grouped_gemm1_combine call on workspace ws
+    (synchronises): microseconds from the kernel start."""
+    v = ws[64:64 + 56].view(torch.int64).cpu().tolist()
+    t0 = v[0]
+    return {"gemm_first_done_us": (v[1] - t0) / 1e3, "gemm_last_done_us": (v[2] - t0) / 1e3,
+            "end_us": (v[3] - t0) / 1e3, "last_push_us": (v[4] - t0) / 1e3,
+            "combine_wait_us_total": v[5] / 1e3, "combine_work_us_total": v[6] / 1e3}
 
 
 def moe_combine(Y: torch.Tensor, layout: Layout, out: torch.Tensor, status: torch.Tensor, stream=None):

@@ -24,6 +24,7 @@ extern "C" int moe_layout_sizes(int T, int k, int E, int G, int block_m, moe_lay
   out->rowmap_len = out->max_tiles * block_m;
   out->layout_ws_bytes = moe_layout_ws_bytes(E);
   out->stage1_ws_bytes = moe_stage1_ws_bytes(T, k, E, block_m);
+  out->gemm_combine_ws_bytes = moe_gemm_combine_ws_bytes(T);
   return MOE_OK;
 }
 

@@ -81,6 +81,7 @@ struct GemmShared {
   uint64_t tempty[2];
   uint64_t ufull[kUnitRing];
   uint64_t uempty[kUnitRing];
+  uint64_t stored[kUnitRing];   // the epilogue warps have stored the unit's Y rows (fused combine)
   uint64_t drain;
   int4 unit[kUnitRing];     // {m (-1: end), nb, expert, row0}
   int unit_rows[kUnitRing];
@@ -126,8 +127,10 @@ MOE_DEV GemmSmem gemm_smem(uint8_t* raw) {
   return g;
 }
 
-// Barrier init + TMEM allocation (whole CTA calls this).
-MOE_DEV void gemm_setup(const GemmSmem& S) {
+// Barrier init + TMEM allocation (whole CTA calls this).  `extra_unit_consumers`
+// warps besides the MMA warp and the epilogue warps read every unit from the
+// ring (and arrive on its empty barrier).
+MOE_DEV void gemm_setup(const GemmSmem& S, int extra_unit_consumers = 0) {
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -141,7 +144,8 @@ MOE_DEV void gemm_setup(const GemmSmem& S) {
     }
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(smem_u32(&sh->ufull[i]), 1);
-      mbar_init(smem_u32(&sh->uempty[i]), 1 + kEpiWarps);
+      mbar_init(smem_u32(&sh->uempty[i]), 1 + kEpiWarps + extra_unit_consumers);
+      mbar_init(smem_u32(&sh->stored[i]), kEpiWarps);
     }
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort_flag = 0;
@@ -297,8 +301,10 @@ struct FoldAcc<true> {
 
 // Promotion + epilogue warps (warps 4..11).  Returns when the end marker arrives.
 // In the fused kernel a unit reaches the ring only after the TMA warp acquired
-// its ready flag, so the A_scale reads here need no wait of their own.
-template <bool kPacked>
+// its ready flag, so the A_scale reads here need no wait of their own.  With
+// kSignal each warp arrives on the unit's `stored` barrier once its Y stores
+// are issued (the fused combine's counting warp takes it from there).
+template <bool kPacked, bool kSignal = false>
 MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -400,6 +406,7 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
       }
       __syncwarp();
     }
+    if (kSignal && lane == 0) mbar_arrive(smem_u32(&sh->stored[slot]));
   }
 }
 

@@ -15,6 +15,8 @@
 size_t moe_layout_ws_bytes(int E);
 // Bytes of the moe_stage1 workspace (defined next to the kernel).
 size_t moe_stage1_ws_bytes(int T, int k, int E, int block_m);
+// Bytes of the moe_grouped_gemm1_combine workspace (defined next to the kernel).
+size_t moe_gemm_combine_ws_bytes(int T);
 
 namespace moe {
 

@@ -76,6 +76,7 @@ typedef struct moe_layout_sizes {
   int64_t rowmap_len;        /* max_tiles * block_m */
   size_t layout_ws_bytes;    /* workspace for moe_route_layout */
   size_t stage1_ws_bytes;    /* workspace for moe_stage1 */
+  size_t gemm_combine_ws_bytes; /* workspace for moe_grouped_gemm1_combine */
 } moe_layout_sizes_t;
 
 int moe_layout_sizes(int T, int k, int E, int G, int block_m, moe_layout_sizes_t* out);
@@ -202,6 +203,37 @@ int moe_grouped_gemm1(const uint8_t* A, const float* A_scale, const uint8_t* W,
  * A pair whose pair_row is -1 contributes nothing. */
 int moe_combine(const uint16_t* Y, int D, const moe_layout_t* L, uint16_t* out, int32_t* status,
                 moe_stream_t stream);
+
+/* moe_grouped_gemm1_combine: moe_grouped_gemm1 and moe_combine (D = N) in one
+ * cooperative launch, the combine of a token overlapping the rest of the GEMM
+ * ([tilepipe] "Overlap": producer and consumer on one GPU synchronised by
+ * per-tile semaphores; its "GEMM -> combine" driver).  After the epilogue
+ * stores a unit's rows, a counting warp bumps a completion counter per token
+ * (release); the bump that completes a token (N/256 per valid pair) puts it on
+ * a ready queue; combining warps (one per CTA during the GEMM, all of a CTA's
+ * warps once its GEMM work is done) pop tokens and write out[t] with the
+ * arithmetic of moe_combine.  Y and out are bit-for-bit what
+ * moe_grouped_gemm1 followed by moe_combine write.
+ *   Arguments as moe_grouped_gemm1, plus out device bf16 [T, N] and ws, a
+ *   device workspace of at least gemm_combine_ws_bytes (16-byte aligned;
+ *   zeroed in-stream by the call).  A token not complete within the bounded
+ *   wait (2 s) writes MOE_ERR_TIMEOUT to *status. */
+/* Trace slots (uint64, ns from %globaltimer) in the gemm1_combine workspace
+ * header, written by every call: kernel start, the first and the last CTA to
+ * finish its GEMM work, kernel end, the last push onto the ready queue, and
+ * the combining warps' total waiting and working time. */
+#define MOE_GC_TRACE_OFFSET 64
+#define MOE_GC_TRACE_START 0
+#define MOE_GC_TRACE_GEMM_FIRST_DONE 1
+#define MOE_GC_TRACE_GEMM_LAST_DONE 2
+#define MOE_GC_TRACE_END 3
+#define MOE_GC_TRACE_LAST_PUSH 4     /* the last token put on the ready queue */
+#define MOE_GC_TRACE_WAIT_NS 5       /* total ns combining warps waited for queued tokens */
+#define MOE_GC_TRACE_WORK_NS 6       /* total ns combining warps spent combining */
+int moe_grouped_gemm1_combine(const uint8_t* A, const float* A_scale, const uint8_t* W,
+                              const float* W_scale, int N, int H, const moe_layout_t* L, uint16_t* Y,
+                              uint16_t* out, void* ws, size_t ws_bytes, int32_t* status,
+                              moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * MXFP8 variant: e8m0 (power-of-two) scales per 32 values, applied by the
