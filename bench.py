@@ -2,9 +2,11 @@
 """Benchmark of the MoE stage1 + combine hot path on GB300.
 
 One step = the whole hot path over one batch of T tokens: routing layout
-(moe_route_layout) -> fused quant + dispatch + GEMM1 (moe_stage1) -> weighted
-combine (moe_combine), all in the library's kernels on one stream, inputs
-resident in HBM.  Default workload: T=8192 tokens, H=7168, 256 experts in 8
+(moe_route_layout) -> quant + dispatch -> GEMM1 -> weighted combine, all in the
+library's kernels on one stream, inputs resident in HBM.  Three variants of
+the step are timed (--variant picks the one behind `value`): unfused
+(moe_dispatch_quant, moe_grouped_gemm1, moe_combine), fused (moe_stage1 +
+moe_combine) and overlap (moe_dispatch_quant + moe_grouped_gemm1_combine).  Default workload: T=8192 tokens, H=7168, 256 experts in 8
 groups, top-8, GEMM1 N=4096, Zipf(1.2) expert popularity (synthetic, seeded).
 
 Prints ONE JSON line (rank 0).  `value` is tokens/s of the step; per-kernel
@@ -191,6 +193,9 @@ class Workload:
         self.out = torch.empty(T, N, dtype=torch.bfloat16, device=device)
         self.ws = torch.empty(int(self.L.sizes.stage1_ws_bytes), dtype=torch.uint8, device=device)
         self.ws_gc = torch.empty(int(self.L.sizes.gemm_combine_ws_bytes), dtype=torch.uint8, device=device)
+        self.runs = moe.SendRuns(self.L, device=device)
+        self.A_send = torch.empty(self.runs.max_rows, H, dtype=torch.uint8, device=device)
+        self.As_send = torch.empty(H // 128, self.runs.max_rows, dtype=torch.float32, device=device)
         self.A_mx = torch.empty(self.R, H, dtype=torch.uint8, device=device)
         self.A_sf = torch.empty(moe.mx_sf_a_shape(self.L, H), dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
@@ -335,6 +340,8 @@ def run_gpu(args):
 
     # ---- the MXFP8 variant on the same step's layout: dispatch and block-scaled GEMM1
     mx = run_mx_variant(wl, s, max(3, args.steps // 2))
+    # ---- the per-(token, group) send runs: their dispatch and GEMM1 gathering A rows
+    runs = run_runs_variant(wl, s, max(3, args.steps // 2))
 
     # ---- end to end through the public API with host buffers: H2D inputs, D2H output
     e2e = run_e2e(wl, s, args, world, device)
@@ -395,6 +402,7 @@ def run_gpu(args):
         "mx": dict(mx, gemm1_tflops=round(wl.gemm_flops() / (mx["gemm1_us"] / 1e6) / 1e12, 1),
                    gemm1_frac_of_burst=round(wl.gemm_flops() / (mx["gemm1_us"] / 1e6) / 1e12 / fp8_burst, 4),
                    dispatch_gbs=round(wl.dispatch_bytes_mx() / (mx["dispatch_us"] / 1e6) / 1e9, 1)),
+        "send_runs": runs,
         "e2e": e2e,
         "gpu_launches": len(parts) * args.steps,
         "clocks": clk,
@@ -407,6 +415,32 @@ def run_gpu(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_runs_variant(wl, s, reps):
+    """The per-(token, group) send runs on the step's layout: the send-run
+    layout, the dispatch into the runs and GEMM1 gathering its A rows from
+    them (median CUDA-event times, the L2 flushed before every launch), with
+    the dispatch's algorithmic bytes beside the dense dispatch's."""
+    moe, c = wl.moe, wl.cfg
+    moe.moe_route_layout(wl.ids, wl.w, wl.L, wl.status, stream=s)
+    lay = _time_events(lambda: moe.moe_send_layout(wl.ids, wl.L, wl.runs, wl.status, stream=s), s, reps, wl.flush)
+    d = _time_events(lambda: moe.moe_dispatch_quant_runs(wl.x, wl.L, wl.runs, wl.A_send, wl.As_send, wl.status,
+                                                         stream=s), s, reps, wl.flush)
+    g = _time_events(lambda: moe.moe_grouped_gemm1_gather(wl.A_send, wl.As_send, wl.Wq, wl.Ws, wl.L, wl.runs, wl.Y,
+                                                          wl.status, stream=s), s, reps, wl.flush)
+    torch.cuda.synchronize()
+    if wl.status.item() != 0:
+        raise RuntimeError(f"device status {moe.status_string(wl.status.item())} in the send-run variant")
+    rows = int(wl.runs["run_offset"][-1].item())
+    bytes_runs = 2.0 * c.T * c.H + rows * c.H + 4.0 * rows * c.H / 128
+    return {"send_rows": rows, "send_rows_per_token": round(rows / c.T, 3), "layout_us": round(lay, 1),
+            "dispatch_us": round(d, 1), "dispatch_bytes": bytes_runs,
+            "dense_dispatch_bytes": wl.dispatch_bytes(),
+            "dispatch_bytes_ratio": round(wl.dispatch_bytes() / bytes_runs, 3),
+            "dispatch_gbs": round(bytes_runs / (d / 1e6) / 1e9, 1),
+            "gemm1_gather_us": round(g, 1),
+            "gemm1_gather_tflops": round(wl.gemm_flops() / (g / 1e6) / 1e12, 1)}
 
 
 def run_mx_variant(wl, s, reps):
@@ -774,8 +808,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="t8192_zipf1.2")
-    ap.add_argument("--variant", choices=VARIANTS, default="overlap",
-                    help="the step timed for `value`; the others are timed beside it")
+    ap.add_argument("--variant", choices=VARIANTS, default="unfused",
+                    help="the step timed for `value` (default: the fastest measured on this workload); the "
+                         "others are timed beside it")
     ap.add_argument("--comm-sms", type=int, default=36)
     ap.add_argument("--flags", type=int, default=0, help="0 per-tile, 1 per-expert")
     ap.add_argument("--schedule", type=int, default=0, help="0 expert-major, 1 ready-first")

@@ -28,7 +28,7 @@ EXPORTS = [
     "moe_grouped_gemm1", "moe_combine", "moe_stage1", "moe_router_topk", "moe_quant_weights",
     "moe_dequant_rows", "moe_device_sm_count", "moe_route_layout_noalloc",
     "moe_dispatch_quant_mx", "moe_quant_weights_mx", "moe_grouped_gemm1_mx", "moe_route_layout_noplan",
-    "moe_grouped_gemm1_combine",
+    "moe_grouped_gemm1_combine", "moe_send_layout", "moe_dispatch_quant_runs", "moe_grouped_gemm1_gather",
 ]
 
 
@@ -41,7 +41,8 @@ class MoEError(RuntimeError):
 class LayoutSizes(ctypes.Structure):
     _fields_ = [("pairs", ctypes.c_int64), ("max_tiles", ctypes.c_int64), ("rowmap_len", ctypes.c_int64),
                 ("layout_ws_bytes", ctypes.c_size_t), ("stage1_ws_bytes", ctypes.c_size_t),
-                ("gemm_combine_ws_bytes", ctypes.c_size_t)]
+                ("gemm_combine_ws_bytes", ctypes.c_size_t), ("max_send_rows", ctypes.c_int64),
+                ("send_ws_bytes", ctypes.c_size_t)]
 
 
 _TABLES = ["count", "expert_offset", "expert_tile_offset", "group_offset", "ready_tokens", "pair_row",
@@ -52,6 +53,13 @@ _TABLES = ["count", "expert_offset", "expert_tile_offset", "group_offset", "read
 class LayoutC(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("T", "k", "E", "G", "block_m", "max_tiles")] + \
                [(n, ctypes.c_void_p) for n in _TABLES]
+
+
+_SEND_TABLES = ["run_offset", "send_token", "send_row", "run_ready", "gather_row"]
+
+
+class SendRunsC(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _SEND_TABLES]
 
 
 class Stage1Opts(ctypes.Structure):
@@ -85,6 +93,11 @@ def lib() -> ctypes.CDLL:
         L.moe_dequant_rows.argtypes = [vp, vp, i32, ctypes.POINTER(LayoutC), vp, vp]
         L.moe_device_sm_count.argtypes = []
         L.moe_route_layout_noalloc.argtypes = [vp, vp, ctypes.POINTER(LayoutC), vp, vp]
+        L.moe_send_layout.argtypes = [vp, ctypes.POINTER(LayoutC), ctypes.POINTER(SendRunsC), vp, sz, vp, vp]
+        L.moe_dispatch_quant_runs.argtypes = [vp, i32, ctypes.POINTER(LayoutC), ctypes.POINTER(SendRunsC), vp, vp,
+                                              vp, vp]
+        L.moe_grouped_gemm1_gather.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(LayoutC), vp,
+                                               ctypes.c_longlong, vp, vp, vp]
         L.moe_grouped_gemm1_combine.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(LayoutC), vp, vp, vp, sz,
                                                 vp, vp]
         L.moe_route_layout_noplan.argtypes = [vp, vp, ctypes.POINTER(LayoutC), vp, vp]
@@ -406,4 +419,69 @@ def moe_grouped_gemm1_mx(A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tensor, W
     _check("moe_grouped_gemm1_mx", lib().moe_grouped_gemm1_mx(
         _ptr(A, torch.uint8, "A"), _ptr(A_sf, torch.uint8, "A_sf"), _ptr(W, torch.uint8, "W"),
         _ptr(W_sf, torch.uint8, "W_sf"), N, H, ctypes.byref(layout.c), _ptr(Y, torch.bfloat16, "Y"),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+# ---------------------------------------------------------------- per-(token, group) send runs
+
+class SendRuns:
+    """Device tables of the send runs of one layout (torch-allocated), their C struct and workspace."""
+
+    def __init__(self, layout: Layout, device="cuda"):
+        T, k, E, G = layout.T, layout.k, layout.E, layout.G
+        s = layout.sizes
+        self.max_rows = int(s.max_send_rows)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.t = {"run_offset": torch.empty(G + 1, **i32), "send_token": torch.empty(self.max_rows, **i32),
+                  "send_row": torch.empty(T * G, **i32), "run_ready": torch.empty(E, **i32),
+                  "gather_row": torch.empty(T * k, **i32)}
+        self.ws = torch.empty(int(s.send_ws_bytes) + 256, dtype=torch.uint8, device=device)
+        off = (-self.ws.data_ptr()) % 256            # the workspace must be 256-byte aligned
+        self.ws_view = self.ws[off:off + int(s.send_ws_bytes)]
+        self.c = SendRunsC(*[self.t[n].data_ptr() for n in _SEND_TABLES])
+
+    def __getitem__(self, name):
+        return self.t[name]
+
+    def numpy(self) -> dict:
+        return {n: v.cpu().numpy() for n, v in self.t.items()}
+
+
+def moe_send_layout(topk_ids: torch.Tensor, layout: Layout, runs: SendRuns, status: torch.Tensor, stream=None):
+    _shape(topk_ids, (layout.T, layout.k), "topk_ids")
+    _status(status)
+    _check("moe_send_layout", lib().moe_send_layout(
+        _ptr(topk_ids, torch.int32, "topk_ids"), ctypes.byref(layout.c), ctypes.byref(runs.c),
+        ctypes.c_void_p(runs.ws_view.data_ptr()), runs.ws_view.numel(), _ptr(status, torch.int32, "status"),
+        _stream(stream)))
+
+
+def moe_dispatch_quant_runs(x: torch.Tensor, layout: Layout, runs: SendRuns, A_send: torch.Tensor,
+                            A_send_scale: torch.Tensor, status: torch.Tensor, stream=None):
+    T, H = _dims(x, 2, "x")
+    _shape(x, (layout.T, H), "x")
+    _shape(A_send, (runs.max_rows, H), "A_send")
+    _shape(A_send_scale, (H // 128, runs.max_rows), "A_send_scale")
+    _status(status)
+    _check("moe_dispatch_quant_runs", lib().moe_dispatch_quant_runs(
+        _ptr(x, torch.bfloat16, "x"), H, ctypes.byref(layout.c), ctypes.byref(runs.c),
+        _ptr(A_send, torch.uint8, "A_send"), _ptr(A_send_scale, torch.float32, "A_send_scale"),
+        _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def moe_grouped_gemm1_gather(A_send: torch.Tensor, A_send_scale: torch.Tensor, W: torch.Tensor,
+                             W_scale: torch.Tensor, layout: Layout, runs: SendRuns, Y: torch.Tensor,
+                             status: torch.Tensor, stream=None):
+    E, N, H = _dims(W, 3, "W")
+    R = layout.T * layout.k
+    _shape(W, (layout.E, N, H), "W")
+    _shape(W_scale, (layout.E, N // 128, H // 128), "W_scale")
+    _shape(A_send, (runs.max_rows, H), "A_send")
+    _shape(A_send_scale, (H // 128, runs.max_rows), "A_send_scale")
+    _shape(Y, (R, N), "Y")
+    _status(status)
+    _check("moe_grouped_gemm1_gather", lib().moe_grouped_gemm1_gather(
+        _ptr(A_send, torch.uint8, "A_send"), _ptr(A_send_scale, torch.float32, "A_send_scale"),
+        _ptr(W, torch.uint8, "W"), _ptr(W_scale, torch.float32, "W_scale"), N, H, ctypes.byref(layout.c),
+        _ptr(runs["gather_row"], torch.int32, "gather_row"), runs.max_rows, _ptr(Y, torch.bfloat16, "Y"),
         _ptr(status, torch.int32, "status"), _stream(stream)))

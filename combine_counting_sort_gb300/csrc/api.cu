@@ -25,6 +25,8 @@ extern "C" int moe_layout_sizes(int T, int k, int E, int G, int block_m, moe_lay
   out->layout_ws_bytes = moe_layout_ws_bytes(E);
   out->stage1_ws_bytes = moe_stage1_ws_bytes(T, k, E, block_m);
   out->gemm_combine_ws_bytes = moe_gemm_combine_ws_bytes(T);
+  out->max_send_rows = moe_max_send_rows(T, k, G);
+  out->send_ws_bytes = moe_send_ws_bytes(T, k, E, G);
   return MOE_OK;
 }
 

@@ -12,6 +12,9 @@
 
 namespace moe {
 
+// kGather: A is read row by row through g.gather_row (per-(token, group) send
+// rows, TMA tile::gather4) instead of as 128-row boxes of the dense buffer.
+template <bool kGather>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm1_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                          const __grid_constant__ GemmParams g) {
@@ -36,7 +39,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
         const Unit x = unit_of(g.L, u, nbn);
         ok = publish_unit(S.sh, j, x, g.status, g.timeout_ns) &&
-             produce_unit(S, &tmA, &tmW, x, KB, it, g.status, g.timeout_ns);
+             (kGather ? produce_unit_gather(S, &tmA, &tmW, g.gather_row, x, KB, it, g.status, g.timeout_ns)
+                      : produce_unit(S, &tmA, &tmW, x, KB, it, g.status, g.timeout_ns));
       }
       if (ok) {
         Unit end = {-1, 0, 0, 0, 0};
@@ -48,7 +52,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     regs_alloc<kRegsEpilogue>();
-    epilogue_loop<true>(S, g);
+    epilogue_loop<true, false, kGather>(S, g);
   }
   gemm_teardown(S);
 }
@@ -57,12 +61,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 using namespace moe;
 
-// Tensor maps of one call: A [R, H] and W [E, N, H], both u8 with 128x128 / 256x128 boxes.
+// Tensor maps of one call: A [R, H] and W [E, N, H], both u8 with 128x128 / 256x128 boxes
+// (A's box one row high when it is gathered).
 static int encode_gemm_maps(const uint8_t* A, const uint8_t* W, long long R, int E, int N, int H,
-                            CUtensorMap* tmA, CUtensorMap* tmW) {
+                            CUtensorMap* tmA, CUtensorMap* tmW, bool gather = false) {
   const uint64_t dA[2] = {(uint64_t)H, (uint64_t)R};
   const uint64_t sA[1] = {(uint64_t)H};
-  const uint32_t bA[2] = {kGemmBK, kGemmBM};
+  const uint32_t bA[2] = {kGemmBK, gather ? 1u : (uint32_t)kGemmBM};
   const uint64_t dW[3] = {(uint64_t)H, (uint64_t)N, (uint64_t)E};
   const uint64_t sW[2] = {(uint64_t)H, (uint64_t)N * H};
   const uint32_t bW[3] = {kGemmBK, kGemmBN, 1};
@@ -102,15 +107,50 @@ extern "C" int moe_grouped_gemm1(const uint8_t* A, const float* A_scale, const u
   g.Y = Y;
   g.status = status;
   g.timeout_ns = 2000000000ull;
+  g.gather_row = nullptr;
   const int nsm = device_sm_count();
   if (nsm <= 0) return MOE_ERR_CUDA;
   const long long max_units = (long long)L->max_tiles * (N / kGemmBN);
   const int grid = (int)std::max(1LL, std::min((long long)nsm, max_units));
-  static const bool split_ok = register_split_fits(grouped_gemm1_kernel);
+  static const bool split_ok = register_split_fits(grouped_gemm1_kernel<false>);
   if (!split_ok) return MOE_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(grouped_gemm1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(grouped_gemm1_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
-  grouped_gemm1_kernel<<<grid, kGemmThreads, kGemmSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, g);
+  grouped_gemm1_kernel<false><<<grid, kGemmThreads, kGemmSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, g);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" int moe_grouped_gemm1_gather(const uint8_t* A_send, const float* A_send_scale, const uint8_t* W,
+                                        const float* W_scale, int N, int H, const moe_layout_t* L,
+                                        const int32_t* gather_row, long long send_rows, uint16_t* Y,
+                                        int32_t* status, moe_stream_t stream) {
+  int rc = gemm1_check_args(A_send, A_send_scale, W, W_scale, N, H, L, Y);
+  if (rc) return rc;
+  if (!gather_row || send_rows < 1 || send_rows >= ((long long)1 << 31)) return MOE_ERR_INVALID_ARG;
+  CUtensorMap tmA, tmW;
+  rc = encode_gemm_maps(A_send, W, send_rows, L->E, N, H, &tmA, &tmW, /*gather=*/true);
+  if (rc) return rc;
+  GemmParams g;
+  g.A_scale = A_send_scale;
+  g.W_scale = W_scale;
+  g.L = to_dev(L);
+  g.N = N;
+  g.H = H;
+  g.R = send_rows;
+  g.Y = Y;
+  g.status = status;
+  g.timeout_ns = 2000000000ull;
+  g.gather_row = gather_row;
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return MOE_ERR_CUDA;
+  const long long max_units = (long long)L->max_tiles * (N / kGemmBN);
+  const int grid = (int)std::max(1LL, std::min((long long)nsm, max_units));
+  static const bool split_ok = register_split_fits(grouped_gemm1_kernel<true>);
+  if (!split_ok) return MOE_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(grouped_gemm1_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kGemmSmemBytes) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  grouped_gemm1_kernel<true><<<grid, kGemmThreads, kGemmSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, g);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

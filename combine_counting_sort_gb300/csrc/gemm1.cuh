@@ -104,10 +104,11 @@ struct GemmParams {
   const float* W_scale;   // [E][N/128][H/128]
   LayoutDev L;
   int N, H;
-  long long R;            // T*k: rows of A / Y
-  uint16_t* Y;            // [R][N]
+  long long R;            // rows of A (the stride of A_scale): T*k, or the send-run capacity
+  uint16_t* Y;            // [T*k][N]
   int32_t* status;
   uint64_t timeout_ns;
+  const int32_t* gather_row;   // [T*k] row of A holding dense row r (gathered A), or null (A dense)
 };
 
 // Shared-memory carve-up: 1024-aligned stage buffers, then the barriers.
@@ -212,6 +213,52 @@ MOE_DEV bool produce_unit(const GemmSmem& S, const CUtensorMap* tmA, const CUten
   return true;
 }
 
+// TMA gather of four rows of a 2-D tensor map whose box is one row high:
+// the rows land at dst as four consecutive 128-byte rows (swizzled like a
+// box of four rows at that address).
+MOE_DEV void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
+                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
+}
+
+// produce_unit with A gathered row by row: dense row row0 + i of the unit is
+// row gather[row0 + i] of A (slots past the unit's rows repeat its first
+// row; their products are never stored).  Lane l gathers slots [4l, 4l + 4) of
+// every K-block with one tile::gather4, so one warp instruction issues the
+// tile's 32 gathers; the elected lane sets the stage's byte count first and
+// loads the W tile.
+MOE_DEV bool produce_unit_gather(const GemmSmem& S, const CUtensorMap* tmA, const CUtensorMap* tmW,
+                                 const int32_t* gather, const Unit& u, int KB, uint32_t& it, int32_t* status,
+                                 uint64_t tmo) {
+  GemmShared* sh = S.sh;
+  const int lane = threadIdx.x & 31;
+  const int first = gather[u.row0];
+  int r4[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int slot = 4 * lane + i;
+    r4[i] = slot < u.rows ? gather[u.row0 + slot] : first;
+  }
+  for (int kb = 0; kb < KB; ++kb) {
+    const int s = (int)(it % kGemmStages);
+    const uint32_t ph = (it / kGemmStages) & 1u;
+    if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, &sh->abort_flag, status, tmo)) return false;
+    const uint32_t full = smem_u32(&sh->full[s]);
+    const uint32_t dstA = smem_u32(S.stages + (size_t)s * kStageBytes);
+    if (elect_one()) mbar_arrive_expect_tx(full, kStageBytes);
+    __syncwarp();
+    tma_gather4(dstA + 512u * (uint32_t)lane, tmA, kb * kGemmBK, r4[0], r4[1], r4[2], r4[3], full);
+    if (elect_one()) tma_load_3d(dstA + kATileBytes, tmW, kb * kGemmBK, u.nb * kGemmBN, u.e, full);
+    __syncwarp();
+    ++it;
+  }
+  return true;
+}
+
 // Before leaving, wait (bounded, ignoring the abort flag) for the last fills in flight.
 MOE_DEV void drain_fills(const GemmSmem& S, uint32_t it, uint64_t tmo) {
   int dummy_abort = 0;
@@ -304,7 +351,7 @@ struct FoldAcc<true> {
 // its ready flag, so the A_scale reads here need no wait of their own.  With
 // kSignal each warp arrives on the unit's `stored` barrier once its Y stores
 // are issued (the fused combine's counting warp takes it from there).
-template <bool kPacked, bool kSignal = false>
+template <bool kPacked, bool kSignal = false, bool kGather = false>
 MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -329,8 +376,11 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
     const bool valid = r_in_tile < rows;
     // Scale addresses as 32-bit element offsets from the parameter bases (no
     // 64-bit pointers live across the K loop).  Rows past the tile's end read
-    // nothing (zero-filled copies) from a clamped, valid address.
-    const uint32_t sa_row = (uint32_t)min((long long)(row0 + r_in_tile), (long long)g.R - 1);
+    // nothing (zero-filled copies) from a clamped, valid address.  With A
+    // gathered, a dense row's scales sit at its row of A.
+    const uint32_t sa_row =
+        kGather ? (uint32_t)(valid ? g.gather_row[row0 + r_in_tile] : 0)
+                : (uint32_t)min((long long)(row0 + r_in_tile), (long long)g.R - 1);
     const uint32_t sa_bytes = valid ? 4u : 0u;
     const uint32_t sb_off = (uint32_t)((e * nsb + nb * 2 + h) * KB);
     FoldAcc<kPacked> acc;

@@ -315,6 +315,7 @@ extern "C" int moe_grouped_gemm1_combine(const uint8_t* A, const float* A_scale,
   g.Y = Y;
   g.status = status;
   g.timeout_ns = 2000000000ull;
+  g.gather_row = nullptr;
   char* base = reinterpret_cast<char*>(ws);
   CombineParams c;
   c.qhead = reinterpret_cast<int32_t*>(base);

@@ -17,6 +17,9 @@ size_t moe_layout_ws_bytes(int E);
 size_t moe_stage1_ws_bytes(int T, int k, int E, int block_m);
 // Bytes of the moe_grouped_gemm1_combine workspace (defined next to the kernel).
 size_t moe_gemm_combine_ws_bytes(int T);
+// Bytes of the moe_send_layout workspace and capacity of the send runs (defined next to the kernels).
+size_t moe_send_ws_bytes(int T, int k, int E, int G);
+long long moe_max_send_rows(int T, int k, int G);
 
 namespace moe {
 

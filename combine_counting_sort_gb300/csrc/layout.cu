@@ -52,6 +52,7 @@ struct LayoutArgs {
   int32_t* status;
   int tpb;              // tokens per block
   uint64_t timeout_ns;
+  int quiet;            // 1: a negative id means "no route" and is skipped without an error status
 };
 
 __device__ __forceinline__ int first_expert(const int32_t* s_ids, int k, int E) {
@@ -191,7 +192,10 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
       int e = -1;
       if (p < q1) {
         e = s_ids[p - q0];
-        if (e < 0 || e >= E) { set_status(a.status, MOE_ERR_EXPERT_ID); e = -1; }
+        if (e < 0 || e >= E) {
+          if (!(a.quiet && e < 0)) set_status(a.status, MOE_ERR_EXPERT_ID);
+          e = -1;
+        }
       }
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[e], __popc(peers));
@@ -447,8 +451,8 @@ size_t moe_layout_ws_bytes(int E) {
 
 // Grid, workspace pointers and launch shared by both entry points.  `ws` is
 // the caller's workspace or the library's fixed scratch.
-static int launch_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L, void* ws,
-                         int32_t* status, cudaStream_t s) {
+int launch_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L, void* ws,
+                  int32_t* status, cudaStream_t s, int quiet) {
   int dev, nsm;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -483,6 +487,7 @@ static int launch_layout(const int32_t* topk_ids, const float* topk_w, const moe
   a.status = status;
   a.tpb = tpb;
   a.timeout_ns = 1000000000ull;
+  a.quiet = quiet;
 
   if (nblk == 1) {
     route_layout_kernel<<<1, kLayoutThreads, smem, s>>>(a);
@@ -513,7 +518,7 @@ extern "C" int moe_route_layout(const int32_t* topk_ids, const float* topk_w, co
   if (!topk_ids || !topk_w || !ws) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < moe_layout_ws_bytes(L->E)) return MOE_ERR_INVALID_ARG;
   if (((uintptr_t)ws & 15) != 0) return MOE_ERR_INVALID_ARG;
-  return launch_layout(topk_ids, topk_w, L, ws, status, (cudaStream_t)stream);
+  return launch_layout(topk_ids, topk_w, L, ws, status, (cudaStream_t)stream, 0);
 }
 
 extern "C" int moe_router_topk(const float* logits, int T, int E, int k, int32_t* topk_ids,
@@ -589,7 +594,7 @@ extern "C" int moe_route_layout_noalloc(const int32_t* topk_ids, const float* to
   void* ws = nullptr;
   rc = layout_scratch_address((cudaStream_t)stream, &ws);
   if (rc) return rc;
-  return launch_layout(topk_ids, topk_w, L, ws, status, (cudaStream_t)stream);
+  return launch_layout(topk_ids, topk_w, L, ws, status, (cudaStream_t)stream, 0);
 }
 
 // ---------------------------------------------------------------- no-plan layout (small batches)

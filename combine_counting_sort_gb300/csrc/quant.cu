@@ -13,21 +13,23 @@ constexpr int kQuantWarps = 8;
 // --split), as many as it takes to give every SM enough warps; each item walks
 // its range chunk by chunk.  Batches below 8192 tokens use 1024-column chunks
 // (more items), larger ones 2048-column chunks (4 KB of the row in flight per warp).
+// `rows` holds per_token destination rows of each token (-1: none), R is the
+// row count of A (the stride of A_scale): the dense layout passes pair_row, k
+// and T*k; the per-(token, group) send runs pass send_row, G and their capacity.
 template <int ROUNDS>
 __global__ void __launch_bounds__(kQuantWarps * 32, ROUNDS == 2 ? 4 : 3) dispatch_quant_kernel(
-    const uint16_t* __restrict__ x, int H, LayoutDev L, int splits, uint8_t* __restrict__ A,
-    float* __restrict__ A_scale) {
+    const uint16_t* __restrict__ x, int H, int T, const int32_t* __restrict__ rows, int per_token, long long R,
+    int splits, uint8_t* __restrict__ A, float* __restrict__ A_scale) {
   constexpr int kSliceCols = 512 * ROUNDS;
   const int lane = threadIdx.x & 31;
-  const int T = L.T, k = L.k;
-  const long long R = (long long)T * k;
+  const int k = per_token;
   const int chunks = (H + kSliceCols - 1) / kSliceCols;
   const int per = (chunks + splits - 1) / splits;
   const long long items = (long long)T * splits;
   for (long long w = (long long)blockIdx.x * kQuantWarps + (threadIdx.x >> 5); w < items;
        w += (long long)gridDim.x * kQuantWarps) {
     const int t = (int)(w / splits), sp = (int)(w % splits);
-    const int myrow = lane < k ? L.pair_row[(size_t)t * k + lane] : -1;
+    const int myrow = lane < k ? rows[(size_t)t * k + lane] : -1;
     const int cend = min(chunks, (sp + 1) * per);
     for (int c = sp * per; c < cend; ++c)
       quant_scatter_slice<ROUNDS>(x, H, t, c * kSliceCols, k, R, myrow, A, A_scale);
@@ -104,6 +106,28 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(const uint8_t* __rest
 
 using namespace moe;
 
+// Launch of the quantise-once scatter over T tokens with `per_token`
+// destination rows each (shared by the dense and the send-run dispatch).
+int launch_dispatch(const uint16_t* x, int H, int T, const int32_t* rows, int per_token, long long R, uint8_t* A,
+                    float* A_scale, cudaStream_t stream) {
+  const int nsm = device_sm_count();
+  if (nsm <= 0) return MOE_ERR_CUDA;
+  // small batches: every 1024-column chunk is an item; large ones: split tokens
+  // only as far as needed for ~64 warps per SM
+  const bool small = T < 8192;
+  const int cols = small ? 1024 : 2048;
+  const int chunks = (H + cols - 1) / cols;
+  const long long want = (long long)nsm * 64;
+  const int splits = small ? chunks : (int)std::max(1LL, std::min((long long)chunks, (want + T - 1) / T));
+  const long long items = (long long)T * splits;
+  const int blocks = (int)std::max(1LL, std::min((items + kQuantWarps - 1) / kQuantWarps, (long long)nsm * 16));
+  if (small)
+    dispatch_quant_kernel<2><<<blocks, kQuantWarps * 32, 0, stream>>>(x, H, T, rows, per_token, R, splits, A, A_scale);
+  else
+    dispatch_quant_kernel<4><<<blocks, kQuantWarps * 32, 0, stream>>>(x, H, T, rows, per_token, R, splits, A, A_scale);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 extern "C" int moe_dispatch_quant(const uint16_t* x, int H, const moe_layout_t* L, uint8_t* A,
                                   float* A_scale, int32_t* status, moe_stream_t stream) {
   (void)status;
@@ -112,22 +136,7 @@ extern "C" int moe_dispatch_quant(const uint16_t* x, int H, const moe_layout_t* 
   if (!x || !A || !A_scale) return MOE_ERR_INVALID_ARG;
   if (H < kQBlock || H % kQBlock != 0 || H > 32768) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(A) || !aligned16(A_scale)) return MOE_ERR_INVALID_ARG;
-  const int nsm = device_sm_count();
-  if (nsm <= 0) return MOE_ERR_CUDA;
-  // small batches: every 1024-column chunk is an item; large ones: split tokens
-  // only as far as needed for ~64 warps per SM
-  const bool small = L->T < 8192;
-  const int cols = small ? 1024 : 2048;
-  const int chunks = (H + cols - 1) / cols;
-  const long long want = (long long)nsm * 64;
-  const int splits = small ? chunks : (int)std::max(1LL, std::min((long long)chunks, (want + L->T - 1) / L->T));
-  const long long items = (long long)L->T * splits;
-  const int blocks = (int)std::max(1LL, std::min((items + kQuantWarps - 1) / kQuantWarps, (long long)nsm * 16));
-  if (small)
-    dispatch_quant_kernel<2><<<blocks, kQuantWarps * 32, 0, (cudaStream_t)stream>>>(x, H, to_dev(L), splits, A, A_scale);
-  else
-    dispatch_quant_kernel<4><<<blocks, kQuantWarps * 32, 0, (cudaStream_t)stream>>>(x, H, to_dev(L), splits, A, A_scale);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_dispatch(x, H, L->T, L->pair_row, L->k, (long long)L->T * L->k, A, A_scale, (cudaStream_t)stream);
 }
 
 extern "C" int moe_quant_weights(const uint16_t* W, int E, int N, int H, uint8_t* Wq, float* W_scale,

@@ -397,6 +397,7 @@ extern "C" int moe_stage1(const uint16_t* x, int H, const moe_layout_t* L, const
   p.g.Y = Y;
   p.g.status = status;
   p.g.timeout_ns = opts->timeout_ns > 0 ? (uint64_t)opts->timeout_ns : 1000000000ull;
+  p.g.gather_row = nullptr;
   p.x = x;
   p.A = A;
   p.A_scale = A_scale;

@@ -77,6 +77,8 @@ typedef struct moe_layout_sizes {
   size_t layout_ws_bytes;    /* workspace for moe_route_layout */
   size_t stage1_ws_bytes;    /* workspace for moe_stage1 */
   size_t gemm_combine_ws_bytes; /* workspace for moe_grouped_gemm1_combine */
+  int64_t max_send_rows;     /* T * min(G, k): capacity of the per-(token, group) send runs */
+  size_t send_ws_bytes;      /* workspace for moe_send_layout */
 } moe_layout_sizes_t;
 
 int moe_layout_sizes(int T, int k, int E, int G, int block_m, moe_layout_sizes_t* out);
@@ -234,6 +236,50 @@ int moe_grouped_gemm1_combine(const uint8_t* A, const float* A_scale, const uint
                               const float* W_scale, int N, int H, const moe_layout_t* L, uint16_t* Y,
                               uint16_t* out, void* ws, size_t ws_bytes, int32_t* status,
                               moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Per-(token, group) send runs: one FP8 row per token and logical group it
+ * routes into ([mori] "What": the sender quantises each token once into a send
+ * buffer grouped by destination; "How it works now": a counting sort by
+ * (destination, first expert) places every token's row so that a landed prefix
+ * of a run is a prefix of experts).  Run g holds one row for every token with
+ * a route into group g, ordered by (the token's smallest expert in g, token);
+ * GEMM1 gathers its A rows from the runs, so the dispatch writes one row per
+ * (token, group) instead of one per (token, slot).  G <= 32.
+ * ------------------------------------------------------------------------- */
+typedef struct moe_send_runs {
+  int32_t* run_offset;   /* [G+1] first send row of run g */
+  int32_t* send_token;   /* [max_send_rows] token held by send row s, -1 past the last */
+  int32_t* send_row;     /* [T*G] send row of (token t, group g), -1 if t has no route into g */
+  int32_t* run_ready;    /* [E] for expert e of group g: end of the prefix of run g that holds
+                            every token routed to e */
+  int32_t* gather_row;   /* [T*k] send row that dense row r of the layout reads, -1 past the
+                            valid rows */
+} moe_send_runs_t;
+
+/* moe_send_layout: the send runs of a routing layout (computed by
+ * moe_route_layout from the same topk_ids).  ws: device workspace of at least
+ * send_ws_bytes, 256-byte aligned (contents ignored).  Ids outside [0, E) are
+ * left out (moe_route_layout reports them). */
+int moe_send_layout(const int32_t* topk_ids, const moe_layout_t* L, const moe_send_runs_t* S, void* ws,
+                    size_t ws_bytes, int32_t* status, moe_stream_t stream);
+
+/* moe_dispatch_quant_runs: quantise each token once (the rule of
+ * moe_dispatch_quant) and store it to its send rows.
+ *   A_send        device u8 [max_send_rows, H]: row send_row[t*G + g] = codes of t.
+ *   A_send_scale  device f32 [H/128, max_send_rows] (block-major, as A_scale). */
+int moe_dispatch_quant_runs(const uint16_t* x, int H, const moe_layout_t* L, const moe_send_runs_t* S,
+                            uint8_t* A_send, float* A_send_scale, int32_t* status, moe_stream_t stream);
+
+/* moe_grouped_gemm1_gather: moe_grouped_gemm1 with A gathered: dense row r of
+ * the layout reads row gather_row[r] of A_send (TMA tile::gather4, four rows
+ * per instruction, the 2-D tensor map's box one row high) and its scales from
+ * A_send_scale at that row.  Y is the dense [T*k, N] output, as
+ * moe_grouped_gemm1's.  send_rows: rows of A_send (max_send_rows). */
+int moe_grouped_gemm1_gather(const uint8_t* A_send, const float* A_send_scale, const uint8_t* W,
+                             const float* W_scale, int N, int H, const moe_layout_t* L,
+                             const int32_t* gather_row, long long send_rows, uint16_t* Y, int32_t* status,
+                             moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * MXFP8 variant: e8m0 (power-of-two) scales per 32 values, applied by the
