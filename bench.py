@@ -37,13 +37,13 @@ if ROOT not in sys.path:
 METRIC = "stage1 µs & tokens/s at T=8192 (GEMM1 TFLOP/s); dispatch/combine HBM GB/s"
 
 # DRAM bytes per launch of the roofline kernel (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# single-pass ncu capture of the full workload, keyed by workload, stage1 variant and a hash of the
-# kernel sources' code (comments aside) the capture ran on.  A kernel changed since then reports null until captured again.
-#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum \
-#       --clock-control none -k regex:stage1_kernel -s 3 -c 1 \
+# single-pass ncu capture of the full workload (the only metrics captured at full size), keyed by workload,
+# step variant and a hash of the code of every kernel source (comments aside).  A kernel changed since then
+# reports null until captured again:
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none \
+#       -k regex:grouped_gemm1_kernel -s 3 -c 1 --csv --log-file traffic.csv \
 #       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-clocks
-KERNEL_SOURCES = ["common.cuh", "gemm1.cuh", "quant.cuh", "stage1.cu", "tmem_fold.cuh"]
-TRAFFIC = {("t8192_zipf1.2", "fused/comm36/per_tile/expert_major/join1", "7f9a65bf9216bc68"): 6.619e9}
+TRAFFIC = {("t8192_zipf1.2", "unfused", "3a788ed3c925d134"): 6.329e9}
 
 
 def kernel_source_hash() -> str:
@@ -51,9 +51,12 @@ def kernel_source_hash() -> str:
     comment edit keeps a capture valid and any code edit invalidates it."""
     import hashlib
     import re
+    import glob
     h = hashlib.sha1()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "combine_counting_sort_gb300", "csrc", f)) as fh:
+    csrc = os.path.join(ROOT, "combine_counting_sort_gb300", "csrc")
+    for path in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
+                       glob.glob(os.path.join(csrc, "*.h"))):
+        with open(path) as fh:
             code = fh.read()
         code = re.sub(r"/\*.*?\*/", "", code, flags=re.S)
         code = re.sub(r"//[^\n]*", "", code)
