@@ -13,11 +13,12 @@
 namespace moe {
 
 // kGather: A is read row by row through g.gather_row (per-(token, group) send
-// rows, TMA tile::gather4) instead of as 128-row boxes of the dense buffer.
+// rows, copied by warps 2 and 3) instead of as 128-row boxes of the dense
+// buffer; `A` is then the send buffer.
 template <bool kGather>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm1_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                         const __grid_constant__ GemmParams g) {
+                         const __grid_constant__ GemmParams g, const uint8_t* A) {
   extern __shared__ uint8_t smem_raw[];
   const GemmSmem S = gemm_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -25,7 +26,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmW);
   }
-  gemm_setup(S);
+  // gathered A: warps 2 and 3 read every unit and each arrive on every stage's full barrier
+  gemm_setup(S, kGather ? 2 : 0, kGather ? 3 : 1);
   const int nbn = g.N / kGemmBN;
   const int KB = g.H / kGemmBK;
   const int units = g.L.num_tiles[0] * nbn;
@@ -39,7 +41,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
         const Unit x = unit_of(g.L, u, nbn);
         ok = publish_unit(S.sh, j, x, g.status, g.timeout_ns) &&
-             (kGather ? produce_unit_gather(S, &tmA, &tmW, g.gather_row, x, KB, it, g.status, g.timeout_ns)
+             (kGather ? produce_unit_w(S, &tmW, x, KB, it, g.status, g.timeout_ns)
                       : produce_unit(S, &tmA, &tmW, x, KB, it, g.status, g.timeout_ns));
       }
       if (ok) {
@@ -49,6 +51,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       drain_fills(S, it, g.timeout_ns);
     } else if (warp == 1) {
       mma_loop(S, KB, g.status, g.timeout_ns);
+    } else if (kGather) {
+      gather_a_loop(S, A, g.gather_row, g.H, KB, g.status, g.timeout_ns);
     }
   } else {
     regs_alloc<kRegsEpilogue>();
@@ -117,7 +121,7 @@ extern "C" int moe_grouped_gemm1(const uint8_t* A, const float* A_scale, const u
   if (cudaFuncSetAttribute(grouped_gemm1_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
-  grouped_gemm1_kernel<false><<<grid, kGemmThreads, kGemmSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, g);
+  grouped_gemm1_kernel<false><<<grid, kGemmThreads, kGemmSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, g, A);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -151,6 +155,6 @@ extern "C" int moe_grouped_gemm1_gather(const uint8_t* A_send, const float* A_se
   if (cudaFuncSetAttribute(grouped_gemm1_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
-  grouped_gemm1_kernel<true><<<grid, kGemmThreads, kGemmSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, g);
+  grouped_gemm1_kernel<true><<<grid, kGemmThreads, kGemmSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, g, A_send);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -131,12 +131,12 @@ MOE_DEV GemmSmem gemm_smem(uint8_t* raw) {
 // Barrier init + TMEM allocation (whole CTA calls this).  `extra_unit_consumers`
 // warps besides the MMA warp and the epilogue warps read every unit from the
 // ring (and arrive on its empty barrier).
-MOE_DEV void gemm_setup(const GemmSmem& S, int extra_unit_consumers = 0) {
+MOE_DEV void gemm_setup(const GemmSmem& S, int extra_unit_consumers = 0, int stage_fillers = 1) {
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGemmStages; ++s) {
-      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->full[s]), stage_fillers);
       mbar_init(smem_u32(&sh->empty[s]), 1);
     }
     for (int p = 0; p < 2; ++p) {
@@ -213,50 +213,93 @@ MOE_DEV bool produce_unit(const GemmSmem& S, const CUtensorMap* tmA, const CUten
   return true;
 }
 
-// TMA gather of four rows of a 2-D tensor map whose box is one row high:
-// the rows land at dst as four consecutive 128-byte rows (swizzled like a
-// box of four rows at that address).
-MOE_DEV void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
-                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
+// 16-byte asynchronous copy global -> shared (zero-filled, nothing read, when
+// src_bytes == 0).
+MOE_DEV void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+               "r"(src_bytes)
+               : "memory");
 }
 
-// produce_unit with A gathered row by row: dense row row0 + i of the unit is
-// row gather[row0 + i] of A (slots past the unit's rows repeat its first
-// row; their products are never stored).  Lane l gathers slots [4l, 4l + 4) of
-// every K-block with one tile::gather4, so one warp instruction issues the
-// tile's 32 gathers; the elected lane sets the stage's byte count first and
-// loads the W tile.
-MOE_DEV bool produce_unit_gather(const GemmSmem& S, const CUtensorMap* tmA, const CUtensorMap* tmW,
-                                 const int32_t* gather, const Unit& u, int KB, uint32_t& it, int32_t* status,
-                                 uint64_t tmo) {
+// Gathered A (per-(token, group) send runs): dense row row0 + i of a unit is
+// row gather[row0 + i] of A.  The TMA warp loads only W (its stage arrival
+// carries W's byte count); warps 2 and 3 copy the A tile 16 bytes at a time
+// (cp.async) into the stage in the 128-byte-swizzled layout the MMA reads
+// (16-byte chunk c of row r at r*128 + (c ^ (r & 7)) * 16), two K-blocks in
+// flight per thread: after committing K-block it they wait for K-block it - 2,
+// make its writes visible to the tensor core (fence.proxy.async) and arrive on
+// its full barrier, which so counts three arrivals (W's and one per gather
+// warp) plus W's bytes.  The lag stays below the stage count, or the warps
+// would wait for a stage that needs their own unsignalled fill.
+constexpr int kGatherLag = 2;
+static_assert(kGatherLag < kGemmStages, "gather lag below the stage count");
+
+MOE_DEV bool produce_unit_w(const GemmSmem& S, const CUtensorMap* tmW, const Unit& u, int KB, uint32_t& it,
+                            int32_t* status, uint64_t tmo) {
   GemmShared* sh = S.sh;
-  const int lane = threadIdx.x & 31;
-  const int first = gather[u.row0];
-  int r4[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int slot = 4 * lane + i;
-    r4[i] = slot < u.rows ? gather[u.row0 + slot] : first;
-  }
   for (int kb = 0; kb < KB; ++kb) {
     const int s = (int)(it % kGemmStages);
     const uint32_t ph = (it / kGemmStages) & 1u;
     if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, &sh->abort_flag, status, tmo)) return false;
-    const uint32_t full = smem_u32(&sh->full[s]);
-    const uint32_t dstA = smem_u32(S.stages + (size_t)s * kStageBytes);
-    if (elect_one()) mbar_arrive_expect_tx(full, kStageBytes);
-    __syncwarp();
-    tma_gather4(dstA + 512u * (uint32_t)lane, tmA, kb * kGemmBK, r4[0], r4[1], r4[2], r4[3], full);
-    if (elect_one()) tma_load_3d(dstA + kATileBytes, tmW, kb * kGemmBK, u.nb * kGemmBN, u.e, full);
+    if (elect_one()) {
+      const uint32_t full = smem_u32(&sh->full[s]);
+      mbar_arrive_expect_tx(full, kBTileBytes);
+      tma_load_3d(smem_u32(S.stages + (size_t)s * kStageBytes) + kATileBytes, tmW, kb * kGemmBK, u.nb * kGemmBN,
+                  u.e, full);
+    }
     __syncwarp();
     ++it;
   }
   return true;
+}
+
+// Gather warps (2 and 3): thread i of the 64 copies rows i and i + 64 of every
+// A tile.  Reads every unit from the ring like the MMA and epilogue warps.
+MOE_DEV void gather_a_loop(const GemmSmem& S, const uint8_t* __restrict__ A, const int32_t* __restrict__ gather,
+                           int H, int KB, int32_t* status, uint64_t tmo) {
+  GemmShared* sh = S.sh;
+  const int lane = threadIdx.x & 31;
+  const int i = (((int)threadIdx.x >> 5) - 2) * 32 + lane;   // 0..63
+  uint32_t it = 0;
+  bool ok = true;
+  for (int j = 0; ok; ++j) {
+    const int slot = j % kUnitRing;
+    if (!mbar_wait(smem_u32(&sh->ufull[slot]), (uint32_t)(j / kUnitRing) & 1u, &sh->abort_flag, status, tmo)) break;
+    const int4 un = sh->unit[slot];
+    const int rows = sh->unit_rows[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sh->uempty[slot]));
+    if (un.x < 0) break;
+    const uint8_t* src0 = A + (size_t)(i < rows ? gather[un.w + i] : 0) * H;
+    const uint8_t* src1 = A + (size_t)(i + 64 < rows ? gather[un.w + i + 64] : 0) * H;
+    const uint32_t n0 = i < rows ? 16u : 0u, n1 = i + 64 < rows ? 16u : 0u;
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = (int)(it % kGemmStages);
+      const uint32_t ph = (it / kGemmStages) & 1u;
+      if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, &sh->abort_flag, status, tmo)) { ok = false; break; }
+      const uint32_t dst = smem_u32(S.stages + (size_t)s * kStageBytes);
+      const uint32_t d0 = dst + (uint32_t)i * 128u, d1 = dst + (uint32_t)(i + 64) * 128u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        cp_async16(d0 + (uint32_t)((c ^ (i & 7)) << 4), src0 + kb * kGemmBK + c * 16, n0);
+        cp_async16(d1 + (uint32_t)((c ^ (i & 7)) << 4), src1 + kb * kGemmBK + c * 16, n1);
+      }
+      cp_async_commit();
+      if (it >= (uint32_t)kGatherLag) {
+        cp_async_wait<kGatherLag>();
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh->full[(it - kGatherLag) % kGemmStages]));
+      }
+      ++it;
+    }
+  }
+  // the fills still in flight: complete, fence, arrive
+  cp_async_wait<0>();
+  fence_proxy_async_shared();
+  __syncwarp();
+  for (uint32_t f = it > (uint32_t)kGatherLag ? it - kGatherLag : 0u; f < it; ++f)
+    if (lane == 0) mbar_arrive(smem_u32(&sh->full[f % kGemmStages]));
 }
 
 // Before leaving, wait (bounded, ignoring the abort flag) for the last fills in flight.
