@@ -29,9 +29,12 @@ def test_reference_line_tiny_workload():
     assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["higher_is_better"] is True
     assert line["steps"] == 3 and line["warmup"] == 3 and line["config"]["workload"] == "tiny"
     assert line["value"] > 0
-    # ms_per_step is the estimated time of one whole step of T tokens
+    # value follows the estimated time of one whole step of T tokens; ms_per_step
+    # is what each sampled step took, so steps x ms_per_step fits the run
     T = inputs.CONFIGS["tiny"].T
-    assert abs(T / (line["ms_per_step"] / 1e3) - line["value"]) <= 0.01 * line["value"] + 0.01
+    assert abs(T / (line["ms_per_full_step_estimate"] / 1e3) - line["value"]) <= 0.01 * line["value"] + 0.01
+    # (seconds_timed is printed to 10 ms, ms_per_step to 0.1 ms)
+    assert line["steps"] * line["ms_per_step"] <= 1e3 * line["cpu_baseline"]["seconds_timed"] + 5.0 + line["steps"]
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
