@@ -29,6 +29,7 @@ EXPORTS = [
     "moe_dequant_rows", "moe_device_sm_count", "moe_route_layout_noalloc",
     "moe_dispatch_quant_mx", "moe_quant_weights_mx", "moe_grouped_gemm1_mx", "moe_route_layout_noplan",
     "moe_grouped_gemm1_combine", "moe_send_layout", "moe_dispatch_quant_runs", "moe_grouped_gemm1_gather",
+    "moe_grouped_gemm1_pair",
 ]
 
 
@@ -85,6 +86,7 @@ def lib() -> ctypes.CDLL:
         L.moe_route_layout.argtypes = [vp, vp, ctypes.POINTER(LayoutC), vp, sz, vp, vp]
         L.moe_dispatch_quant.argtypes = [vp, i32, ctypes.POINTER(LayoutC), vp, vp, vp, vp]
         L.moe_grouped_gemm1.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(LayoutC), vp, vp, vp]
+        L.moe_grouped_gemm1_pair.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(LayoutC), vp, vp, vp]
         L.moe_combine.argtypes = [vp, i32, ctypes.POINTER(LayoutC), vp, vp, vp]
         L.moe_stage1.argtypes = [vp, i32, ctypes.POINTER(LayoutC), vp, vp, i32, ctypes.POINTER(Stage1Opts),
                                  vp, vp, vp, vp, sz, vp, vp]
@@ -244,7 +246,9 @@ def moe_dispatch_quant(x: torch.Tensor, layout: Layout, A: torch.Tensor, A_scale
 
 
 def moe_grouped_gemm1(A: torch.Tensor, A_scale: torch.Tensor, W: torch.Tensor, W_scale: torch.Tensor,
-                      layout: Layout, Y: torch.Tensor, status: torch.Tensor, stream=None):
+                      layout: Layout, Y: torch.Tensor, status: torch.Tensor, stream=None, pair: bool = False):
+    """GEMM1 over the layout's M-tiles; pair=True runs it on CTA pairs
+    (moe_grouped_gemm1_pair: M = 256 MMAs over two SMs, same Y)."""
     E, N, H = _dims(W, 3, "W")
     R = layout.T * layout.k
     _shape(W, (layout.E, N, H), "W")
@@ -253,7 +257,8 @@ def moe_grouped_gemm1(A: torch.Tensor, A_scale: torch.Tensor, W: torch.Tensor, W
     _shape(A_scale, (H // 128, R), "A_scale")
     _shape(Y, (R, N), "Y")
     _status(status)
-    _check("moe_grouped_gemm1", lib().moe_grouped_gemm1(
+    name = "moe_grouped_gemm1_pair" if pair else "moe_grouped_gemm1"
+    _check(name, getattr(lib(), name)(
         _ptr(A, torch.uint8, "A"), _ptr(A_scale, torch.float32, "A_scale"), _ptr(W, torch.uint8, "W"),
         _ptr(W_scale, torch.float32, "W_scale"), N, H, ctypes.byref(layout.c), _ptr(Y, torch.bfloat16, "Y"),
         _ptr(status, torch.int32, "status"), _stream(stream)))

@@ -16,9 +16,10 @@
 //                    of expert e) into a 4-stage ring, 128-byte swizzled.
 //   warp 1           (converged; one elected lane issues) 4 tcgen05.mma (K=32
 //                    each, M=128, N=256, e4m3 x e4m3 -> fp32) per K-block into
-//                    one of two TMEM partial buffers (2 x 256 columns) and one
-//                    commit to that buffer's partial-ready barrier; the
-//                    promotion warps hand the smem stage back when they see it.
+//                    one of two TMEM partial buffers (2 x 256 columns), one
+//                    commit to the smem stage's empty barrier (the stage goes
+//                    back to the TMA thread as soon as the MMAs that read it
+//                    are done) and one to that buffer's partial-ready barrier.
 //   warps 2, 3       idle (they complete warpgroup 0, whose registers go to
 //                    the promotion warpgroups: setmaxnreg 40 / 232).
 //   warps 4..11      promotion: each thread owns one row (TMEM lane) and 128
@@ -43,6 +44,11 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 256;
 constexpr int kGemmBK = 128;
 constexpr int kGemmStages = 4;
+// CTA pairs (M = 256 over two SMs): a stage holds this CTA's 128 rows of A and
+// its 128 of the unit's 256 W rows, 32 KiB, so six fit where four single-CTA
+// stages do.
+constexpr int kPairStages = 6;
+constexpr int kGemmMaxStages = 6;
 constexpr int kScaleAhead = 4;   // K-blocks of block scales the promotion warps fetch ahead
 constexpr int kGemmThreads = 384;
 constexpr int kEpiWarps = 8;
@@ -75,8 +81,8 @@ constexpr uint32_t kTmemCols = 512;                   // two fp32 partial buffer
 constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kGemmBM, kGemmBN);
 
 struct GemmShared {
-  uint64_t full[kGemmStages];
-  uint64_t empty[kGemmStages];
+  uint64_t full[kGemmMaxStages];
+  uint64_t empty[kGemmMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t ufull[kUnitRing];
@@ -342,8 +348,8 @@ MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) 
         for (int k4 = 0; k4 < kGemmBK / 32; ++k4)
           umma_f8f6f4(tmem + p * kGemmBN, sw128_kmajor_desc(a0 + k4 * 32), sw128_kmajor_desc(b0 + k4 * 32),
                       kIdesc, k4 > 0 ? 1u : 0u);
-        // one commit per K-block: the promotion warps release the smem stage
-        // (empty[s]) when they see the partial, i.e. when these MMAs are done
+        // the stage is free once these MMAs are done; the partial is ready then too
+        umma_commit(smem_u32(&sh->empty[s]));
         umma_commit(smem_u32(&sh->tfull[p]));
       }
       __syncwarp();
@@ -394,7 +400,10 @@ struct FoldAcc<true> {
 // its ready flag, so the A_scale reads here need no wait of their own.  With
 // kSignal each warp arrives on the unit's `stored` barrier once its Y stores
 // are issued (the fused combine's counting warp takes it from there).
-template <bool kPacked, bool kSignal = false, bool kGather = false>
+// With kPair the CTA is one of a pair running M = 256 MMAs: a TMEM partial is
+// free again once both CTAs' warps have loaded it, so every promotion warp
+// reports to the even CTA's barrier.
+template <bool kPacked, bool kSignal = false, bool kGather = false, bool kPair = false>
 MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -457,14 +466,17 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
       cp_async_commit();
       const uint32_t p = pit & 1u, pph = (pit >> 1) & 1u;
       if (!mbar_wait(smem_u32(&sh->tfull[p]), pph, &sh->abort_flag, g.status, g.timeout_ns)) return;
-      // the MMAs that read smem stage (pit % stages) are complete: hand the stage back to the TMA thread
-      if (warp == kEpiWarp0 && lane == 0) mbar_arrive(smem_u32(&sh->empty[pit % kGemmStages]));
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + p * kGemmBN + h * 128;
       acc.fold(taddr, sc);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[p]));
+      if (lane == 0) {
+        if (kPair)   // the even CTA's barrier, from either CTA
+          mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&sh->tempty[p]), 0));
+        else
+          mbar_arrive(smem_u32(&sh->tempty[p]));
+      }
       ++pit;
     }
     // bf16 output through the warp's staging tile: lane = row on the way in,

@@ -197,6 +197,16 @@ int moe_grouped_gemm1(const uint8_t* A, const float* A_scale, const uint8_t* W,
                       const float* W_scale, int N, int H, const moe_layout_t* L, uint16_t* Y,
                       int32_t* status, moe_stream_t stream);
 
+/* moe_grouped_gemm1_pair: moe_grouped_gemm1 on CTA pairs.  Same arguments,
+ * same Y (the same fp32 partials folded in the same order).  A 2-CTA cluster
+ * runs tcgen05 MMAs of M = 256 (two consecutive M-tiles of one expert; the
+ * second empty when the expert has an odd tile count) against 256 columns,
+ * each SM holding its 128 rows of A and 128 of the 256 W rows.
+ * MOE_ERR_UNSUPPORTED on a device with fewer than two SMs. */
+int moe_grouped_gemm1_pair(const uint8_t* A, const float* A_scale, const uint8_t* W,
+                           const float* W_scale, int N, int H, const moe_layout_t* L, uint16_t* Y,
+                           int32_t* status, moe_stream_t stream);
+
 /* moe_combine: out[t, :] = bf16( sum_{j<k} w[t,j] * Y[pair_row[t*k+j], :] ),
  * accumulated in fp32 with the slots in ascending order; w is read as
  * row_weight[pair_row[t*k+j]] ([tilepipe] "Communication Kernels": the
