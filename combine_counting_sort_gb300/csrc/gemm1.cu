@@ -13,8 +13,9 @@
 namespace moe {
 
 // kGather: A is read row by row through g.gather_row (per-(token, group) send
-// rows, copied by warps 2 and 3) instead of as 128-row boxes of the dense
-// buffer; `A` is then the send buffer.
+// rows; half the tile rows gathered by the TMA warp, half copied by warps 2
+// and 3) instead of as 128-row boxes of the dense buffer; `A` is then the
+// send buffer.
 template <bool kGather>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm1_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
@@ -26,8 +27,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmW);
   }
-  // gathered A: warps 2 and 3 read every unit and each arrive on every stage's full barrier
-  gemm_setup(S, kGather ? 2 : 0, kGather ? 3 : 1);
+  // gathered A: warps 2 and 3 read every unit; one of them arrives on each stage's full barrier
+  gemm_setup(S, kGather ? 2 : 0, kGather ? 2 : 1);
   const int nbn = g.N / kGemmBN;
   const int KB = g.H / kGemmBK;
   const int units = g.L.num_tiles[0] * nbn;
@@ -41,7 +42,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
         const Unit x = unit_of(g.L, u, nbn);
         ok = publish_unit(S.sh, j, x, g.status, g.timeout_ns) &&
-             (kGather ? produce_unit_w(S, &tmW, x, KB, it, g.status, g.timeout_ns)
+             (kGather ? produce_unit_gather(S, &tmA, &tmW, g.gather_row, x, KB, it, g.status, g.timeout_ns)
                       : produce_unit(S, &tmA, &tmW, x, KB, it, g.status, g.timeout_ns));
       }
       if (ok) {

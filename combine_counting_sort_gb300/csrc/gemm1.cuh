@@ -228,44 +228,78 @@ MOE_DEV void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
 }
 
 // Gathered A (per-(token, group) send runs): dense row row0 + i of a unit is
-// row gather[row0 + i] of A.  The TMA warp loads only W (its stage arrival
-// carries W's byte count); warps 2 and 3 copy the A tile 16 bytes at a time
-// (cp.async) into the stage in the 128-byte-swizzled layout the MMA reads
-// (16-byte chunk c of row r at r*128 + (c ^ (r & 7)) * 16), two K-blocks in
-// flight per thread: after committing K-block it they wait for K-block it - 2,
-// make its writes visible to the tensor core (fence.proxy.async) and arrive on
-// its full barrier, which so counts three arrivals (W's and one per gather
-// warp) plus W's bytes.  The lag stays below the stage count, or the warps
-// would wait for a stage that needs their own unsignalled fill.
-constexpr int kGatherLag = 2;
-static_assert(kGatherLag < kGemmStages, "gather lag below the stage count");
+// row gather[row0 + i] of A.  A row slice of a K-block is 128 bytes, and two
+// engines fetch them side by side: the TMA warp gathers tile rows [0, 64)
+// with tile::gather4 (16 lanes, four rows each, the tensor map's box one row
+// high; the copy engine swizzles each row by its shared-memory address), and
+// warps 2 and 3 copy rows [64, 128) 16 bytes at a time with cp.async into the
+// same 128-byte-swizzled layout (16-byte chunk c of row r at
+// r*128 + (c ^ (r & 7)) * 16).  Either engine alone moves too few rows per
+// K-block (the copy engine takes tens of cycles per row request, the
+// load/store path a few tens of bytes per clock).  A stage's full barrier
+// counts the TMA warp's arrival with W's and the gathered rows' bytes, plus
+// one arrival from the gather warp that filled its other half: warp 2 fills
+// the even stages of the CTA's sequence, warp 3 the odd ones, each waiting
+// for its own copies, making them visible to the tensor core
+// (fence.proxy.async) and arriving before it moves on.
+constexpr int kGatherTmaRows = 64;
+constexpr int kGatherCopyRows = kGemmBM - kGatherTmaRows;
+static_assert(kGatherTmaRows % 4 == 0 && kGatherTmaRows / 4 <= 32 && kGatherCopyRows % 32 == 0,
+              "gather split: whole gather4 lanes, whole warps of copied rows");
 
-MOE_DEV bool produce_unit_w(const GemmSmem& S, const CUtensorMap* tmW, const Unit& u, int KB, uint32_t& it,
-                            int32_t* status, uint64_t tmo) {
+// TMA gather of four rows of a 2-D tensor map whose box is one row high: the
+// rows land at dst as four consecutive 128-byte rows.
+MOE_DEV void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
+                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
+}
+
+// TMA warp, gathered A: W tile plus tile rows [0, kGatherTmaRows) (slots past
+// the unit's rows repeat its first row; their products are never stored).
+MOE_DEV bool produce_unit_gather(const GemmSmem& S, const CUtensorMap* tmA, const CUtensorMap* tmW,
+                                 const int32_t* __restrict__ gather, const Unit& u, int KB, uint32_t& it,
+                                 int32_t* status, uint64_t tmo) {
   GemmShared* sh = S.sh;
+  const int lane = threadIdx.x & 31;
+  const int first = gather[u.row0];
+  int r4[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int slot = 4 * (lane % (kGatherTmaRows / 4)) + q;
+    r4[q] = slot < u.rows ? gather[u.row0 + slot] : first;
+  }
   for (int kb = 0; kb < KB; ++kb) {
     const int s = (int)(it % kGemmStages);
     const uint32_t ph = (it / kGemmStages) & 1u;
     if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, &sh->abort_flag, status, tmo)) return false;
+    const uint32_t full = smem_u32(&sh->full[s]);
+    const uint32_t dstA = smem_u32(S.stages + (size_t)s * kStageBytes);
     if (elect_one()) {
-      const uint32_t full = smem_u32(&sh->full[s]);
-      mbar_arrive_expect_tx(full, kBTileBytes);
-      tma_load_3d(smem_u32(S.stages + (size_t)s * kStageBytes) + kATileBytes, tmW, kb * kGemmBK, u.nb * kGemmBN,
-                  u.e, full);
+      mbar_arrive_expect_tx(full, kBTileBytes + kGatherTmaRows * kGemmBK);
+      tma_load_3d(dstA + kATileBytes, tmW, kb * kGemmBK, u.nb * kGemmBN, u.e, full);
     }
+    __syncwarp();
+    if (lane < kGatherTmaRows / 4)
+      tma_gather4(dstA + 512u * (uint32_t)lane, tmA, kb * kGemmBK, r4[0], r4[1], r4[2], r4[3], full);
     __syncwarp();
     ++it;
   }
   return true;
 }
 
-// Gather warps (2 and 3): thread i of the 64 copies rows i and i + 64 of every
-// A tile.  Reads every unit from the ring like the MMA and epilogue warps.
+// Gather warps (2 and 3): lane l copies tile rows kGatherTmaRows + l + 32 m of
+// the K-blocks of its parity.  Reads every unit from the ring like the MMA and
+// epilogue warps.
 MOE_DEV void gather_a_loop(const GemmSmem& S, const uint8_t* __restrict__ A, const int32_t* __restrict__ gather,
                            int H, int KB, int32_t* status, uint64_t tmo) {
+  constexpr int kM = kGatherCopyRows / 32;
   GemmShared* sh = S.sh;
   const int lane = threadIdx.x & 31;
-  const int i = (((int)threadIdx.x >> 5) - 2) * 32 + lane;   // 0..63
+  const uint32_t par = (((int)threadIdx.x >> 5) - 2) & 1u;
   uint32_t it = 0;
   bool ok = true;
   for (int j = 0; ok; ++j) {
@@ -276,36 +310,36 @@ MOE_DEV void gather_a_loop(const GemmSmem& S, const uint8_t* __restrict__ A, con
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&sh->uempty[slot]));
     if (un.x < 0) break;
-    const uint8_t* src0 = A + (size_t)(i < rows ? gather[un.w + i] : 0) * H;
-    const uint8_t* src1 = A + (size_t)(i + 64 < rows ? gather[un.w + i + 64] : 0) * H;
-    const uint32_t n0 = i < rows ? 16u : 0u, n1 = i + 64 < rows ? 16u : 0u;
-    for (int kb = 0; kb < KB; ++kb) {
+    const uint8_t* src[kM];
+    uint32_t nbytes[kM];
+#pragma unroll
+    for (int m = 0; m < kM; ++m) {
+      const int r = kGatherTmaRows + lane + 32 * m;
+      src[m] = A + (size_t)(r < rows ? gather[un.w + r] : 0) * H;
+      nbytes[m] = r < rows ? 16u : 0u;
+    }
+    for (int kb = 0; kb < KB; ++kb, ++it) {
+      if ((it & 1u) != par) continue;
       const int s = (int)(it % kGemmStages);
       const uint32_t ph = (it / kGemmStages) & 1u;
       if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, &sh->abort_flag, status, tmo)) { ok = false; break; }
       const uint32_t dst = smem_u32(S.stages + (size_t)s * kStageBytes);
-      const uint32_t d0 = dst + (uint32_t)i * 128u, d1 = dst + (uint32_t)(i + 64) * 128u;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        cp_async16(d0 + (uint32_t)((c ^ (i & 7)) << 4), src0 + kb * kGemmBK + c * 16, n0);
-        cp_async16(d1 + (uint32_t)((c ^ (i & 7)) << 4), src1 + kb * kGemmBK + c * 16, n1);
+      for (int m = 0; m < kM; ++m) {
+        const int r = kGatherTmaRows + lane + 32 * m;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          cp_async16(dst + (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4), src[m] + kb * kGemmBK + c * 16,
+                     nbytes[m]);
       }
       cp_async_commit();
-      if (it >= (uint32_t)kGatherLag) {
-        cp_async_wait<kGatherLag>();
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh->full[(it - kGatherLag) % kGemmStages]));
-      }
-      ++it;
+      cp_async_wait<0>();
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->full[s]));
     }
   }
-  // the fills still in flight: complete, fence, arrive
   cp_async_wait<0>();
-  fence_proxy_async_shared();
-  __syncwarp();
-  for (uint32_t f = it > (uint32_t)kGatherLag ? it - kGatherLag : 0u; f < it; ++f)
-    if (lane == 0) mbar_arrive(smem_u32(&sh->full[f % kGemmStages]));
 }
 
 // Before leaving, wait (bounded, ignoring the abort flag) for the last fills in flight.

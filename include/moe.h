@@ -282,10 +282,11 @@ int moe_dispatch_quant_runs(const uint16_t* x, int H, const moe_layout_t* L, con
                             uint8_t* A_send, float* A_send_scale, int32_t* status, moe_stream_t stream);
 
 /* moe_grouped_gemm1_gather: moe_grouped_gemm1 with A gathered: dense row r of
- * the layout reads row gather_row[r] of A_send (16-byte cp.async copies into
- * the swizzled shared-memory stage) and its scales from A_send_scale at that
- * row.  Y is the dense [T*k, N] output, as
- * moe_grouped_gemm1's.  send_rows: rows of A_send (max_send_rows). */
+ * the layout reads row gather_row[r] of A_send (half of each tile's rows by
+ * TMA tile::gather4, half by 16-byte cp.async copies, into the swizzled
+ * shared-memory stage) and its scales from A_send_scale at that row.  Y is
+ * the dense [T*k, N] output, as moe_grouped_gemm1's.  send_rows: rows of
+ * A_send (max_send_rows). */
 int moe_grouped_gemm1_gather(const uint8_t* A_send, const float* A_send_scale, const uint8_t* W,
                              const float* W_scale, int N, int H, const moe_layout_t* L,
                              const int32_t* gather_row, long long send_rows, uint16_t* Y, int32_t* status,
