@@ -43,7 +43,7 @@ METRIC = "stage1 µs & tokens/s at T=8192 (GEMM1 TFLOP/s); dispatch/combine HBM 
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none \
 #       -k regex:grouped_gemm1_kernel -s 3 -c 1 --csv --log-file traffic.csv \
 #       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-clocks
-TRAFFIC = {("t8192_zipf1.2", "unfused", "3a788ed3c925d134"): 6.329e9}
+TRAFFIC = {("t8192_zipf1.2", "unfused", "55358214de0aea59"): 6.387e9}
 
 
 def kernel_source_hash() -> str:
@@ -345,6 +345,8 @@ def run_gpu(args):
     mx = run_mx_variant(wl, s, max(3, args.steps // 2))
     # ---- the per-(token, group) send runs: their dispatch and GEMM1 gathering A rows
     runs = run_runs_variant(wl, s, max(3, args.steps // 2))
+    # ---- GEMM1 on CTA pairs (cta_group::2) on the same dispatch buffer
+    pair = run_pair_variant(wl, s, max(3, args.steps // 2))
 
     # ---- end to end through the public API with host buffers: H2D inputs, D2H output
     e2e = run_e2e(wl, s, args, world, device)
@@ -406,6 +408,9 @@ def run_gpu(args):
                    gemm1_frac_of_burst=round(wl.gemm_flops() / (mx["gemm1_us"] / 1e6) / 1e12 / fp8_burst, 4),
                    dispatch_gbs=round(wl.dispatch_bytes_mx() / (mx["dispatch_us"] / 1e6) / 1e9, 1)),
         "send_runs": runs,
+        "gemm1_pair": dict(pair, gemm1_tflops=round(wl.gemm_flops() / (pair["gemm1_us"] / 1e6) / 1e12, 1),
+                           gemm1_frac_of_burst=round(wl.gemm_flops() / (pair["gemm1_us"] / 1e6) / 1e12 / fp8_burst,
+                                                     4)),
         "e2e": e2e,
         "gpu_launches": len(parts) * args.steps,
         "clocks": clk,
@@ -461,6 +466,27 @@ def run_mx_variant(wl, s, reps):
         raise RuntimeError(f"device status {moe.status_string(wl.status.item())} in the MX variant")
     return {"dispatch_us": round(d, 1), "gemm1_us": round(g, 1),
             "scales": "e8m0 per 32 values (amax/448 rounded up to a power of two), applied by the tensor core"}
+
+
+def run_pair_variant(wl, s, reps):
+    """GEMM1 on CTA pairs (tcgen05 cta_group::2, M = 256 over two SMs) on the
+    step's dispatch buffer: median CUDA-event time over `reps` launches, the L2
+    flushed before every launch; its Y must be the single-CTA kernel's."""
+    moe = wl.moe
+    moe.moe_route_layout(wl.ids, wl.w, wl.L, wl.status, stream=s)
+    moe.moe_dispatch_quant(wl.x, wl.L, wl.A, wl.As, wl.status, stream=s)
+    moe.moe_grouped_gemm1(wl.A, wl.As, wl.Wq, wl.Ws, wl.L, wl.Y, wl.status, stream=s)
+    with torch.cuda.stream(s):
+        Y1 = wl.Y.clone()
+    g = _time_events(lambda: moe.moe_grouped_gemm1(wl.A, wl.As, wl.Wq, wl.Ws, wl.L, wl.Y, wl.status, stream=s,
+                                                    pair=True), s, reps, wl.flush)
+    torch.cuda.synchronize()
+    if wl.status.item() != 0:
+        raise RuntimeError(f"device status {moe.status_string(wl.status.item())} in the pair GEMM1")
+    same = bool(torch.equal(Y1.view(torch.int16), wl.Y.view(torch.int16)))
+    del Y1
+    return {"gemm1_us": round(g, 1), "same_Y_as_single_cta": same,
+            "pairs": "two M-tiles of one expert x 256 columns per 2-CTA cluster (odd tile counts leave one CTA empty)"}
 
 
 def run_e2e(wl, s, args, world, device):

@@ -352,7 +352,11 @@ MOE_DEV void drain_fills(const GemmSmem& S, uint32_t it, uint64_t tmo) {
 
 // MMA warp (all 32 lanes run the loop; one elected lane issues the tcgen05
 // instructions, so descriptors and addresses stay warp-uniform): consume units
-// until the end marker.
+// until the end marker.  kCommitRelease: a commit after the K-block's MMAs
+// hands its smem stage back (the standalone GEMM1 kernels); otherwise the
+// first promotion warp does when it sees the partial (epilogue_loop's
+// kReleaseStage; the fused kernels, where that measured faster).
+template <bool kCommitRelease = true>
 MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) {
   GemmShared* sh = S.sh;
   const uint32_t tmem = sh->tmem_base;
@@ -383,7 +387,7 @@ MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) 
           umma_f8f6f4(tmem + p * kGemmBN, sw128_kmajor_desc(a0 + k4 * 32), sw128_kmajor_desc(b0 + k4 * 32),
                       kIdesc, k4 > 0 ? 1u : 0u);
         // the stage is free once these MMAs are done; the partial is ready then too
-        umma_commit(smem_u32(&sh->empty[s]));
+        if (kCommitRelease) umma_commit(smem_u32(&sh->empty[s]));
         umma_commit(smem_u32(&sh->tfull[p]));
       }
       __syncwarp();
@@ -436,8 +440,10 @@ struct FoldAcc<true> {
 // are issued (the fused combine's counting warp takes it from there).
 // With kPair the CTA is one of a pair running M = 256 MMAs: a TMEM partial is
 // free again once both CTAs' warps have loaded it, so every promotion warp
-// reports to the even CTA's barrier.
-template <bool kPacked, bool kSignal = false, bool kGather = false, bool kPair = false>
+// reports to the even CTA's barrier.  With kReleaseStage the first promotion
+// warp hands the K-block's smem stage back when it sees the partial (paired
+// with mma_loop<false>).
+template <bool kPacked, bool kSignal = false, bool kGather = false, bool kPair = false, bool kReleaseStage = false>
 MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -500,6 +506,8 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
       cp_async_commit();
       const uint32_t p = pit & 1u, pph = (pit >> 1) & 1u;
       if (!mbar_wait(smem_u32(&sh->tfull[p]), pph, &sh->abort_flag, g.status, g.timeout_ns)) return;
+      // the MMAs that read smem stage (pit % stages) are complete: hand the stage back to the TMA thread
+      if (kReleaseStage && warp == kEpiWarp0 && lane == 0) mbar_arrive(smem_u32(&sh->empty[pit % kGemmStages]));
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + p * kGemmBN + h * 128;
       acc.fold(taddr, sc);
