@@ -45,8 +45,8 @@ struct LayoutArgs {
   const int32_t* ids;
   const float* w;
   LayoutDev L;
-  int32_t* ws_hist;     // [nblk][E]
-  int32_t* ws_fhist;    // [nblk][E]
+  int32_t* ws_hist;     // [E][kLayoutMaxBlocks]: expert e's count in block b at e * kLayoutMaxBlocks + b
+  int32_t* ws_fhist;    // [E][kLayoutMaxBlocks]
   int32_t* ws_tot;      // [2][E] column totals of ws_hist / ws_fhist
   uint32_t* ws_barrier; // [2] zeroed in-stream before the launch
   int32_t* status;
@@ -91,33 +91,35 @@ __device__ bool grid_barrier(uint32_t* ctr, int nblk, int32_t* status, uint64_t 
   return *flag == 0;
 }
 
-// One warp scans column `col` (stride E, nblk <= 256 entries) in place into
-// exclusive prefixes and returns the column total (all lanes).
-__device__ int warp_column_scan(int32_t* col, int E, int nblk) {
+// One warp scans column `col` (nblk <= 256 contiguous entries) in place into
+// exclusive prefixes and returns the column total (all lanes).  Rows of 32
+// entries, one coalesced load per row: each row's warp scan on top of the
+// rows before it.
+__device__ int warp_column_scan(int32_t* col, int nblk) {
   const int lane = threadIdx.x & 31;
-  const int per = (nblk + 31) / 32;     // <= 8
+  const int rows = (nblk + 31) / 32;     // <= 8
   int v[8];
-  int sum = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int bb = lane * per + i;
-    v[i] = (i < per && bb < nblk) ? __ldcg(col + (size_t)bb * E) : 0;
-    sum += v[i];
+    const int bb = i * 32 + lane;
+    v[i] = (i < rows && bb < nblk) ? __ldcg(col + bb) : 0;
   }
-  int incl = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  int run = incl - sum;
+  int base = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int bb = lane * per + i;
-    if (i < per && bb < nblk) col[(size_t)bb * E] = run;
-    run += v[i];
+    if (i < rows) {
+      int incl = v[i];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      const int bb = i * 32 + lane;
+      if (bb < nblk) col[bb] = base + incl - v[i];
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
   }
-  return __shfl_sync(0xffffffffu, incl, 31);
+  return base;
 }
 
 // Exclusive scan over n <= 2*blockDim values held in shared memory (in place),
@@ -225,8 +227,8 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
     }
   } else {
     for (int e = tid; e < E; e += blockDim.x) {
-      a.ws_hist[(size_t)b * E + e] = hist[e];
-      a.ws_fhist[(size_t)b * E + e] = fhist[e];
+      a.ws_hist[(size_t)e * kLayoutMaxBlocks + b] = hist[e];
+      a.ws_fhist[(size_t)e * kLayoutMaxBlocks + b] = fhist[e];
     }
 
     // ---------------- phase B1: scan every expert column down the blocks (one warp per column)
@@ -234,8 +236,8 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
     {
       const int nwarps = blockDim.x >> 5;
       for (int item = b * nwarps + warp; item < 2 * E; item += nblk * nwarps) {
-        int32_t* col = (item < E ? a.ws_hist : a.ws_fhist) + (item % E);
-        const int total = warp_column_scan(col, E, nblk);
+        int32_t* col = (item < E ? a.ws_hist : a.ws_fhist) + (size_t)(item % E) * kLayoutMaxBlocks;
+        const int total = warp_column_scan(col, nblk);
         if (lane == 0) a.ws_tot[item] = total;
       }
     }
@@ -244,8 +246,8 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
     // ---------------- phase B2: this block's prefixes, expert scans
     for (int e = tid; e < E; e += blockDim.x) {
       const int tot = __ldcg(a.ws_tot + e), ftot = __ldcg(a.ws_tot + E + e);
-      hist[e] = __ldcg(a.ws_hist + (size_t)b * E + e);     // this block's first row within expert e (relative)
-      fhist[e] = __ldcg(a.ws_fhist + (size_t)b * E + e);   // this block's first position within first-expert e
+      hist[e] = __ldcg(a.ws_hist + (size_t)e * kLayoutMaxBlocks + b);     // this block's first row within expert e (relative)
+      fhist[e] = __ldcg(a.ws_fhist + (size_t)e * kLayoutMaxBlocks + b);   // this block's first position within first-expert e
       eoff[e] = tot;
       toff[e] = (tot + BM - 1) / BM;
       foff[e] = ftot;
