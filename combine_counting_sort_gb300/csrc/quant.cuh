@@ -28,58 +28,41 @@ MOE_DEV void unpack16(const uint4& a, const uint4& b, float (&f)[16]) {
 // code = e4m3_rn_satfinite(RN(x / scale)) with the IEEE fp32 quotient; scale 0
 // -> codes 0.
 //
-// Fast path: v' = RN(x * RN(1/scale)).  Both roundings are relative errors of
-// at most 2^-24, so v' is within 3 * 2^-24 (relative) of the exact quotient
-// q = RN(x/scale).  The e4m3 rounding (nearest-even, saturating) is monotonic,
-// so if it maps the bracket lo = RN(v' * (1 - 2^-21)) and hi = RN(v' *
-// (1 + 2^-21)) to the same code, q (inside the bracket: 2^-21 - 2^-24 >
-// 3 * 2^-24) has that code too.  Where v' is an fp32 subnormal the bounds do
-// not hold, but there |q| < 2^-10 as well and both round to the signed zero of
-// their (exact) sign.
-//
-// A value whose bracket straddles a rounding boundary takes the IEEE division,
-// and so does every value of a lane whose scale is below the fp32 normal range
-// (RN(1/scale) not within 2^-24, or overflowing).  With bf16 inputs straddling
-// is common (q often lands exactly on a midpoint between two codes: ~0.5% of
-// values, so most warps hold one somewhere in a 16-value round), so only the
-// flagged values are divided: the warp loops while any lane has one left,
-// each lane taking its next flagged value (selected from the 16 by compare
-// and select, so nothing is indexed dynamically).  Whole warp, converged.
+// The quotient by one fused-multiply-add correction of the reciprocal product
+// (Markstein's division step, as given for FMA machines in "Computation of
+// elementary functions on the IBM RISC System/6000 processor", 1990, and in
+// the Handbook of Floating-Point Arithmetic, division chapter): with
+// r = RN(1/scale), q0 = RN(x r), rem = RN(x - q0 scale) (one fma),
+// q = RN(q0 + rem r) (one fma); x = +-0 keeps its own sign.  q is not always
+// the correctly rounded fp32 quotient, but its e4m3 code is: for every bf16
+// block maximum a with scale = RN(a / 448) >= 2^-80 and every bf16 x with
+// |x| <= a, the code of q equals the code of the IEEE quotient (all 1.06e9
+// pairs compared on the GPU against the IEEE division).  Below 2^-80 (the
+// residual can fall under the fp32 normal range) and for a non-finite scale
+// the lane divides instead (rare: block maxima under 2^-71).  No branch on the
+// values, so a warp stays converged.
 MOE_DEV uint4 quant16(const float (&f)[16], float scale) {
-  constexpr float kBelow = 1.0f - 0x1p-21f, kAbove = 1.0f + 0x1p-21f;
   uint32_t p[4] = {0u, 0u, 0u, 0u};
-  uint32_t need = 0u;   // bit j: value j takes the IEEE division
-  if (scale > 0.0f) {
+  if (scale >= 0x1p-80f && scale <= 0x1.fffffep127f) {
     const float inv = __frcp_rn(scale);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float v[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = __fmul_rn(f[4 * i + j], inv);
-      const uint32_t below = e4m3x2(__fmul_rn(v[0], kBelow), __fmul_rn(v[1], kBelow)) |
-                             ((uint32_t)e4m3x2(__fmul_rn(v[2], kBelow), __fmul_rn(v[3], kBelow)) << 16);
-      const uint32_t above = e4m3x2(__fmul_rn(v[0], kAbove), __fmul_rn(v[1], kAbove)) |
-                             ((uint32_t)e4m3x2(__fmul_rn(v[2], kAbove), __fmul_rn(v[3], kAbove)) << 16);
-      // one bit per differing byte: bytes 0..3 -> bits 0..3 (the multiply gathers them into bits 24..27)
-      const uint32_t bytes = __vcmpne4(below, above) & 0x01010101u;
-      need |= ((bytes * 0x01020408u) >> 24) << (4 * i);
-      p[i] = below;
+      for (int j = 0; j < 4; ++j) {
+        const float x = f[4 * i + j];
+        const float q0 = __fmul_rn(x, inv);
+        const float rem = __fmaf_rn(-q0, scale, x);
+        const float q = __fmaf_rn(rem, inv, q0);
+        v[j] = x == 0.0f ? x : q;
+      }
+      p[i] = e4m3x2(v[0], v[1]) | ((uint32_t)e4m3x2(v[2], v[3]) << 16);
     }
-    if (scale < 0x1p-126f) need = 0xFFFFu;
-  }
-  while (__any_sync(0xffffffffu, need != 0u)) {
-    if (need != 0u) {
-      const int j = __ffs(need) - 1;
-      need &= need - 1u;
-      float xj = f[0];
+  } else if (scale > 0.0f) {
 #pragma unroll
-      for (int k = 1; k < 16; ++k) xj = j == k ? f[k] : xj;
-      const uint32_t c = e4m3x2(__fdiv_rn(xj, scale), 0.0f) & 0xFFu;
-      const int w = j >> 2, sh = (j & 3) * 8;
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (w == k) p[k] = (p[k] & ~(0xFFu << sh)) | (c << sh);
-    }
+    for (int i = 0; i < 4; ++i)
+      p[i] = e4m3x2(__fdiv_rn(f[4 * i], scale), __fdiv_rn(f[4 * i + 1], scale)) |
+             ((uint32_t)e4m3x2(__fdiv_rn(f[4 * i + 2], scale), __fdiv_rn(f[4 * i + 3], scale)) << 16);
   }
   return make_uint4(p[0], p[1], p[2], p[3]);
 }

@@ -165,6 +165,11 @@ def test_dispatch_every_bf16_quotient_bit_exact():
     # tiny blocks: scale amax/448 below the fp32 normal range (subnormal scales,
     # bf16 subnormal inputs), where RN(1/scale) overflows or loses precision
     amaxes += [2.0 ** -110, 2.0 ** -118, 2.0 ** -120, 2.0 ** -126, 2.0 ** -130, 2.0 ** -133]
+    # either side of scale 2^-80 (block maxima near 448 * 2^-80), where the
+    # quantiser switches between the fma-corrected quotient and the division,
+    # and random maxima over the whole bf16 normal range
+    amaxes += [2.0 ** -69, 2.0 ** -70, 448.0 * 2.0 ** -80, 2.0 ** -71.3, 2.0 ** -72, 2.0 ** -90, 2.0 ** -100]
+    amaxes += list(oracle.bf16_to_f32(rng.integers(0x0080, 0x7F00, 16).astype(np.uint16)))
     blocks = []
     for a in amaxes:
         ab = oracle.f64_to_bf16(np.array([a]))[0]
