@@ -37,9 +37,10 @@ if ROOT not in sys.path:
 METRIC = "stage1 µs & tokens/s at T=8192 (GEMM1 TFLOP/s); dispatch/combine HBM GB/s"
 
 # DRAM bytes per launch of the roofline kernel (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# single-pass ncu capture of the full workload (the only metrics captured at full size), keyed by workload,
-# step variant and a hash of the code of every kernel source (comments aside).  A kernel changed since then
-# reports null until captured again:
+# single-pass ncu capture of the full workload (the only metrics captured at full size: ncu reports
+# "1 pass" for this metric set on the small profile_t8192_e32 workload, so nothing is saved or restored
+# around the launch), keyed by workload, step variant and a hash of the code of every kernel source
+# (comments aside).  A kernel changed since then reports null until captured again:
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none \
 #       -k regex:grouped_gemm1_kernel -s 3 -c 1 --csv --log-file traffic.csv \
 #       python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-clocks
