@@ -78,6 +78,31 @@ MOE_DEV float block_amax8(const float (&f)[16]) {
   return am;
 }
 
+// The slice's block scales to the token's k rows with every lane storing: a
+// round's 4 scales sit in lanes 0, 8, 16, 24 (sc[r]); lane l takes row
+// l / 4 (of each group of 8 rows) and block l % 4 of every round, so one
+// store instruction covers 8 rows x 4 blocks instead of 4 lanes' worth.
+template <int ROUNDS>
+MOE_DEV void store_block_scales(const float (&sc)[ROUNDS], int H, int c0, int k, long long R, int myrow,
+                                float* __restrict__ A_scale) {
+  const int lane = threadIdx.x & 31;
+  const int part = lane & 3;
+  float v[ROUNDS];
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) v[r] = __shfl_sync(0xffffffffu, sc[r], 8 * part);
+  for (int jb = 0; jb < k; jb += 8) {
+    const int j = jb + (lane >> 2);
+    const int row = __shfl_sync(0xffffffffu, myrow, j & 31);
+    if (j < k && row >= 0) {
+#pragma unroll
+      for (int r = 0; r < ROUNDS; ++r) {
+        const int col = c0 + r * 512 + part * kQBlock;
+        if (col < H) A_scale[(size_t)(col / kQBlock) * R + row] = v[r];
+      }
+    }
+  }
+}
+
 // One slice [c0, c0 + 512*ROUNDS) of token t (the mori page's --split: a
 // token's hidden dimension shared by several warps): all 2*ROUNDS 16-byte
 // loads of the lane are issued before any arithmetic, so each warp keeps
@@ -109,6 +134,7 @@ MOE_DEV void quant_scatter_slice(const uint16_t* __restrict__ x, int H, int t, i
     sc[r] = __fdiv_rn(block_amax8(f), 448.0f);
     q[r] = quant16(f, sc[r]);
   }
+  store_block_scales<ROUNDS>(sc, H, c0, k, R, myrow, A_scale);
   for (int j = 0; j < k; ++j) {
     const int row = __shfl_sync(0xffffffffu, myrow, j);
     if (row < 0) continue;
@@ -116,10 +142,7 @@ MOE_DEV void quant_scatter_slice(const uint16_t* __restrict__ x, int H, int t, i
 #pragma unroll
     for (int r = 0; r < ROUNDS; ++r) {
       const int col = c0 + r * 512 + lane * 16;
-      if (col < H) {
-        *reinterpret_cast<uint4*>(arow + col) = q[r];
-        if ((lane & 7) == 0) A_scale[(size_t)(col / kQBlock) * R + row] = sc[r];
-      }
+      if (col < H) *reinterpret_cast<uint4*>(arow + col) = q[r];
     }
   }
 }
@@ -156,15 +179,7 @@ MOE_DEV void quant_stage_slice(const uint16_t* __restrict__ x, int H, int t, int
                    "r"(q.z), "r"(q.w)
                    : "memory");
   }
-  for (int j = 0; j < k; ++j) {
-    const int row = __shfl_sync(0xffffffffu, myrow, j);
-    if (row < 0) continue;
-#pragma unroll
-    for (int r = 0; r < ROUNDS; ++r) {
-      const int col = c0 + r * 512 + lane * 16;
-      if (col < H && (lane & 7) == 0) A_scale[(size_t)(col / kQBlock) * R + row] = sc[r];
-    }
-  }
+  store_block_scales<ROUNDS>(sc, H, c0, k, R, myrow, A_scale);
 }
 
 }  // namespace moe
