@@ -16,10 +16,16 @@ namespace moe {
 // rows; half the tile rows gathered by the TMA warp, half copied by warps 2
 // and 3) instead of as 128-row boxes of the dense buffer; `A` is then the
 // send buffer.
+// A maps with boxes 32 and 64 rows high, for tiles with that few rows (dense A).
+struct ShortMaps {
+  CUtensorMap m[2];
+};
+
 template <bool kGather>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm1_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                         const __grid_constant__ GemmParams g, const uint8_t* A) {
+                         const __grid_constant__ ShortMaps tmS, const __grid_constant__ GemmParams g,
+                         const uint8_t* A) {
   extern __shared__ uint8_t smem_raw[];
   const GemmSmem S = gemm_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -43,7 +49,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const Unit x = unit_of(g.L, u, nbn);
         ok = publish_unit(S.sh, j, x, g.status, g.timeout_ns) &&
              (kGather ? produce_unit_gather(S, &tmA, &tmW, g.gather_row, x, KB, it, g.status, g.timeout_ns)
-                      : produce_unit(S, &tmA, &tmW, x, KB, it, g.status, g.timeout_ns));
+                      : produce_unit(S, &tmA, &tmW, x, KB, it, g.status, g.timeout_ns, tmS.m));
       }
       if (ok) {
         Unit end = {-1, 0, 0, 0, 0};
@@ -102,6 +108,13 @@ extern "C" int moe_grouped_gemm1(const uint8_t* A, const float* A_scale, const u
   CUtensorMap tmA, tmW;
   rc = encode_gemm_maps(A, W, R, L->E, N, H, &tmA, &tmW);
   if (rc) return rc;
+  ShortMaps tmS;
+  for (int i = 0; i < 2; ++i) {
+    const uint64_t dA[2] = {(uint64_t)H, (uint64_t)R};
+    const uint64_t sA[1] = {(uint64_t)H};
+    const uint32_t bA[2] = {kGemmBK, i == 0 ? 32u : 64u};
+    if (!encode_u8_map(&tmS.m[i], A, 2, dA, sA, bA)) return MOE_ERR_CUDA;
+  }
   GemmParams g;
   g.A_scale = A_scale;
   g.W_scale = W_scale;
@@ -122,7 +135,7 @@ extern "C" int moe_grouped_gemm1(const uint8_t* A, const float* A_scale, const u
   if (cudaFuncSetAttribute(grouped_gemm1_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
-  grouped_gemm1_kernel<false><<<grid, kGemmThreads, kGemmSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, g, A);
+  grouped_gemm1_kernel<false><<<grid, kGemmThreads, kGemmSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, tmS, g, A);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -156,6 +169,10 @@ extern "C" int moe_grouped_gemm1_gather(const uint8_t* A_send, const float* A_se
   if (cudaFuncSetAttribute(grouped_gemm1_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGemmSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
-  grouped_gemm1_kernel<true><<<grid, kGemmThreads, kGemmSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, g, A_send);
+  ShortMaps unused;   // the gathered path loads A row by row
+  unused.m[0] = tmA;
+  unused.m[1] = tmA;
+  grouped_gemm1_kernel<true><<<grid, kGemmThreads, kGemmSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, unused, g,
+                                                                                           A_send);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

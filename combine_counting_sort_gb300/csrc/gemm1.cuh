@@ -198,19 +198,31 @@ MOE_DEV bool publish_unit(GemmShared* sh, int j, const Unit& u, int32_t* status,
 }
 
 // Producer warp: stream the K-blocks of one unit into the stage ring.  `it`
-// counts stage fills.
+// counts stage fills.  With `tmA_short` (maps whose boxes are 32 and 64 rows
+// high), a tile of at most 32 (64) valid rows loads only that many A rows:
+// the MMA still reads all 128 rows of the stage, but rows past the tile's
+// end only feed output rows that are never stored, so whatever the stage
+// held there before does not matter, and the short box saves shared-memory
+// and L2 traffic on the experts with few rows.
 MOE_DEV bool produce_unit(const GemmSmem& S, const CUtensorMap* tmA, const CUtensorMap* tmW,
-                          const Unit& u, int KB, uint32_t& it, int32_t* status, uint64_t tmo) {
+                          const Unit& u, int KB, uint32_t& it, int32_t* status, uint64_t tmo,
+                          const CUtensorMap* tmA_short = nullptr) {
   GemmShared* sh = S.sh;
+  const CUtensorMap* mapA = tmA;
+  uint32_t a_bytes = kATileBytes;
+  if (tmA_short != nullptr && u.rows <= 64) {
+    mapA = u.rows <= 32 ? tmA_short : tmA_short + 1;
+    a_bytes = (u.rows <= 32 ? 32u : 64u) * kGemmBK;
+  }
   for (int kb = 0; kb < KB; ++kb) {
     const int s = (int)(it % kGemmStages);
     const uint32_t ph = (it / kGemmStages) & 1u;
     if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, &sh->abort_flag, status, tmo)) return false;
     if (elect_one()) {
       const uint32_t full = smem_u32(&sh->full[s]);
-      mbar_arrive_expect_tx(full, kStageBytes);
+      mbar_arrive_expect_tx(full, a_bytes + kBTileBytes);
       const uint32_t dstA = smem_u32(S.stages + (size_t)s * kStageBytes);
-      tma_load_2d(dstA, tmA, kb * kGemmBK, u.row0, full);
+      tma_load_2d(dstA, mapA, kb * kGemmBK, u.row0, full);
       tma_load_3d(dstA + kATileBytes, tmW, kb * kGemmBK, u.nb * kGemmBN, u.e, full);
     }
     __syncwarp();
