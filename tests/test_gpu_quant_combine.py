@@ -41,6 +41,39 @@ def test_dispatch_matches_oracle_bit_exact(name):
     assert np.array_equal(As.cpu().numpy().view(np.uint32), As_ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("T,H,E,G,k", [
+    (64, 1152, 4, 2, 1),      # one row per token; H not a multiple of 512 (ragged rounds)
+    (200, 640, 16, 4, 5),     # k not a multiple of 8
+    (300, 1152, 32, 8, 12),   # block scales stored in two groups of 8 rows
+    (130, 384, 64, 8, 32),    # the largest k: four groups of 8 rows
+    (8300, 256, 24, 4, 12),   # the large-batch dispatch (4 rounds per slice), k > 8
+])
+def test_dispatch_k_and_widths_bit_exact(T, H, E, G, k):
+    rng = np.random.default_rng(T + k)
+    x = inputs.make_x(T, H, seed=k)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    ids[3, k // 2] = -1                      # a skipped pair: its row is absent
+    w = np.full((T, k), 1.0 / k, np.float32)
+    L, status = gu.gpu_layout(ids, w, E, G)
+    assert status.item() == moe.MOE_ERR_EXPERT_ID
+    R = T * k
+    A = torch.full((R, H), 0x7F, dtype=torch.uint8, device="cuda")
+    As = torch.full((H // 128, R), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_dispatch_quant(x.cuda(), L, A, As, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    q, s = oracle.quantize_rows(inputs.bf16_bits(x))
+    pair_row = L["pair_row"].cpu().numpy()
+    valid = int(L["expert_offset"][-1].item())
+    A_ref, As_ref = oracle.dispatch(q, s, pair_row, k)
+    assert np.array_equal(A.cpu().numpy()[:valid], A_ref[:valid])
+    assert np.array_equal(As.cpu().numpy()[:, :valid].view(np.uint32), As_ref[:, :valid].view(np.uint32))
+    # rows past the valid ones (the skipped pair's) were never written
+    assert np.all(A.cpu().numpy()[valid:] == 0x7F)
+    assert np.isnan(As.cpu().numpy()[:, valid:]).all()
+
+
 def test_dispatch_special_blocks_bit_exact():
     # zero blocks, constant blocks, signed zeros, exact grid values, subnormal-range values, ragged T
     T, H, E, G, k = 45, 640, 6, 3, 3

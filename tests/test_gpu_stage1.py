@@ -112,6 +112,14 @@ def test_stage1_wide_rows():
         P.check_same_as_unfused(opts)
 
 
+def test_stage1_k12_bit_identical_to_unfused():
+    # k > 8: the producers' block scales go out in two groups of 8 rows
+    cfg = inputs.MoEConfig("k12", T=400, H=512, E=48, G=4, k=12, N=256, zipf=1.1, seed=12)
+    P = Problem(cfg)
+    for opts in (moe.stage1_opts(comm_sms=8), moe.stage1_opts(comm_sms=24, flags=moe.MOE_FLAGS_PER_EXPERT)):
+        P.check_same_as_unfused(opts)
+
+
 def test_stage1_full_size_bit_identical_to_unfused():
     # the benchmark's step configuration and two others at T=8192
     P = Problem(inputs.CONFIGS["t8192_zipf1.2"])
