@@ -97,6 +97,13 @@ MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Two fp32 values as one packed pair (lo in the low half), the operand form of the .f32x2 instructions.
+MOE_DEV unsigned long long pack_f32x2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
 // A packed pair of fp32 values (low half first) -> two bf16 values.
 MOE_DEV uint32_t pack_bf16x2_from_pair(unsigned long long v) {
   return pack_bf16x2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));

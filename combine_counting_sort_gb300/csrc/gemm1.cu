@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                          const uint8_t* A) {
   extern __shared__ uint8_t smem_raw[];
   const GemmSmem S = gemm_smem(smem_raw);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmW);
@@ -57,13 +57,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       drain_fills(S, it, g.timeout_ns);
     } else if (warp == 1) {
-      mma_loop(S, KB, g.status, g.timeout_ns);
+      mma_loop<true, !kGather>(S, KB, g.status, g.timeout_ns);
     } else if (kGather) {
       gather_a_loop(S, A, g.gather_row, g.H, KB, g.status, g.timeout_ns);
     }
   } else {
     regs_alloc<kRegsEpilogue>();
-    epilogue_loop<true, false, kGather>(S, g);
+    epilogue_loop<true, false, kGather, false, false, !kGather>(S, g);
   }
   gemm_teardown(S);
 }

@@ -79,6 +79,14 @@ constexpr uint32_t kBTileBytes = kGemmBN * kGemmBK;   // 32 KiB
 constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
 constexpr uint32_t kTmemCols = 512;                   // two fp32 partial buffers of 256 columns
 constexpr uint32_t kIdesc = idesc_f8_e4m3_f32(kGemmBM, kGemmBN);
+// Transposed units: a tile of at most kSwapRows valid rows is computed as
+// Y^T = W A^T, the unit's 256 W rows as two M = 128 operands and its rows as
+// one N = kSwapRows operand (the 32-row A box), so the tensor core reads 8 KB
+// of A per K-block instead of 16 and the promotion warps fold 32 columns per
+// thread instead of 128.  The partial of W half h sits at TMEM columns
+// [h * kSwapRows, +kSwapRows) of the K-block's buffer, lane = W row.
+constexpr int kSwapRows = 32;
+constexpr uint32_t kIdescSwap = idesc_f8_e4m3_f32(kGemmBM, kSwapRows);
 
 struct GemmShared {
   uint64_t full[kGemmMaxStages];
@@ -367,8 +375,10 @@ MOE_DEV void drain_fills(const GemmSmem& S, uint32_t it, uint64_t tmo) {
 // until the end marker.  kCommitRelease: a commit after the K-block's MMAs
 // hands its smem stage back (the standalone GEMM1 kernels); otherwise the
 // first promotion warp does when it sees the partial (epilogue_loop's
-// kReleaseStage; the fused kernels, where that measured faster).
-template <bool kCommitRelease = true>
+// kReleaseStage; the fused kernels, where that measured faster).  kSwap: units
+// of at most kSwapRows rows run transposed (the producer loads their A rows
+// as the 32-row box).
+template <bool kCommitRelease = true, bool kSwap = false>
 MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) {
   GemmShared* sh = S.sh;
   const uint32_t tmem = sh->tmem_base;
@@ -379,6 +389,7 @@ MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) 
     if (!mbar_wait(smem_u32(&sh->ufull[slot]), (uint32_t)(j / kUnitRing) & 1u, &sh->abort_flag, status, tmo))
       break;
     const int m = sh->unit[slot].x;
+    const bool swap = kSwap && sh->unit_rows[slot] <= kSwapRows;
     __syncwarp();
     if (elect_one()) mbar_arrive(smem_u32(&sh->uempty[slot]));
     if (m < 0) break;
@@ -394,10 +405,20 @@ MOE_DEV void mma_loop(const GemmSmem& S, int KB, int32_t* status, uint64_t tmo) 
       const uint32_t a0 = smem_u32(S.stages + (size_t)s * kStageBytes);
       const uint32_t b0 = a0 + kATileBytes;
       if (elect_one()) {
+        if (swap) {
 #pragma unroll
-        for (int k4 = 0; k4 < kGemmBK / 32; ++k4)
-          umma_f8f6f4(tmem + p * kGemmBN, sw128_kmajor_desc(a0 + k4 * 32), sw128_kmajor_desc(b0 + k4 * 32),
-                      kIdesc, k4 > 0 ? 1u : 0u);
+          for (int k4 = 0; k4 < kGemmBK / 32; ++k4)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              umma_f8f6f4(tmem + p * kGemmBN + h * kSwapRows,
+                          sw128_kmajor_desc(b0 + h * (kBTileBytes / 2) + k4 * 32), sw128_kmajor_desc(a0 + k4 * 32),
+                          kIdescSwap, k4 > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int k4 = 0; k4 < kGemmBK / 32; ++k4)
+            umma_f8f6f4(tmem + p * kGemmBN, sw128_kmajor_desc(a0 + k4 * 32), sw128_kmajor_desc(b0 + k4 * 32),
+                        kIdesc, k4 > 0 ? 1u : 0u);
+        }
         // the stage is free once these MMAs are done; the partial is ready then too
         if (kCommitRelease) umma_commit(smem_u32(&sh->empty[s]));
         umma_commit(smem_u32(&sh->tfull[p]));
@@ -432,6 +453,9 @@ struct FoldAcc<false> {
   }
   MOE_DEV void fold(uint32_t taddr, float sc) { tmem_fold128(taddr, sc, v); }
   MOE_DEV uint32_t bf16x2(int c) const { return pack_bf16x2(v[c], v[c + 1]); }   // columns c, c + 1
+  // transposed units take the packed form only (epilogue_loop asserts it)
+  MOE_DEV void fold_cols(uint32_t, const unsigned long long (&)[16]) {}
+  MOE_DEV float col(int t) const { return v[t]; }
 };
 
 template <>
@@ -443,6 +467,9 @@ struct FoldAcc<true> {
   }
   MOE_DEV void fold(uint32_t taddr, float sc) { tmem_fold128x2(taddr, sc, v); }
   MOE_DEV uint32_t bf16x2(int c) const { return pack_bf16x2_from_pair(v[c / 2]); }   // c even
+  // transposed unit: 32 token columns with their own scales into v[0..15]
+  MOE_DEV void fold_cols(uint32_t taddr, const unsigned long long (&c)[16]) { tmem_fold32x2(taddr, c, v); }
+  MOE_DEV float col(int t) const { return __uint_as_float((t & 1) ? (uint32_t)(v[t / 2] >> 32) : (uint32_t)v[t / 2]); }
 };
 
 // Promotion + epilogue warps (warps 4..11).  Returns when the end marker arrives.
@@ -454,9 +481,14 @@ struct FoldAcc<true> {
 // free again once both CTAs' warps have loaded it, so every promotion warp
 // reports to the even CTA's barrier.  With kReleaseStage the first promotion
 // warp hands the K-block's smem stage back when it sees the partial (paired
-// with mma_loop<false>).
-template <bool kPacked, bool kSignal = false, bool kGather = false, bool kPair = false, bool kReleaseStage = false>
+// with mma_loop<false>).  With kSwap, units of at most kSwapRows rows arrive
+// transposed (mma_loop<..., true>): each thread folds its W row's 32 token
+// columns, with the 32 tokens' A scales from the warp's scale ring, and
+// stores one output column.
+template <bool kPacked, bool kSignal = false, bool kGather = false, bool kPair = false, bool kReleaseStage = false,
+          bool kSwap = false>
 MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
+  static_assert(!kSwap || (kPacked && !kGather && !kPair), "transposed units: packed fold, dense A, one CTA");
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                 // TMEM lane quarter this warp may access
@@ -477,14 +509,18 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
     if (lane == 0) mbar_arrive(smem_u32(&sh->uempty[slot]));
     if (un.x < 0) return;
     const int nb = un.y, e = un.z, row0 = un.w;
-    const bool valid = r_in_tile < rows;
+    const bool swap = kSwap && rows <= kSwapRows;
+    // the A row whose scales this thread fetches: its own row, or in a
+    // transposed unit the token of its lane (the warp shares all 32)
+    const int r_scale = swap ? lane : r_in_tile;
+    const bool valid = r_scale < rows;
     // Scale addresses as 32-bit element offsets from the parameter bases (no
     // 64-bit pointers live across the K loop).  Rows past the tile's end read
     // nothing (zero-filled copies) from a clamped, valid address.  With A
     // gathered, a dense row's scales sit at its row of A.
     const uint32_t sa_row =
         kGather ? (uint32_t)(valid ? g.gather_row[row0 + r_in_tile] : 0)
-                : (uint32_t)min((long long)(row0 + r_in_tile), (long long)g.R - 1);
+                : (uint32_t)min((long long)(row0 + r_scale), (long long)g.R - 1);
     const uint32_t sa_bytes = valid ? 4u : 0u;
     const uint32_t sb_off = (uint32_t)((e * nsb + nb * 2 + h) * KB);
     FoldAcc<kPacked> acc;
@@ -492,37 +528,39 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
     // Block scales kScaleAhead K-blocks ahead (they come from L2): each thread
     // keeps its own ring of (sa, sb) pairs in the warp's staging tile, filled
     // by cp.async, so no register waits on a load in flight; one commit group
-    // per K-block (empty past the end).
+    // per K-block (empty past the end).  Slot i is the 256 bytes at
+    // stg_s + i * 256: (sa, sb) of lane l at 8 l, or in a transposed unit the
+    // 32 tokens' sa in the first 128 bytes and each lane's copy of sb after.
     uint8_t* stg = S.out_stage + (size_t)(warp - kEpiWarp0) * kOutStageBytes;
     const uint32_t stg_s = smem_u32(stg);
-    const uint32_t ring = stg_s + lane * 8;           // slot i at ring + i * 256
+    const uint32_t sa_dst = stg_s + (swap ? lane * 4u : lane * 8u);
+    const uint32_t sb_dst = stg_s + (swap ? 128u + lane * 4u : lane * 8u + 4u);
 #pragma unroll
     for (int i = 0; i < kScaleAhead; ++i) {
       if (i < KB) {
-        cp_async4(ring + i * 256, g.A_scale + (size_t)i * g.R + sa_row, sa_bytes);
-        cp_async4(ring + i * 256 + 4, g.W_scale + sb_off + i, 4u);
+        cp_async4(sa_dst + i * 256, g.A_scale + (size_t)i * g.R + sa_row, sa_bytes);
+        cp_async4(sb_dst + i * 256, g.W_scale + sb_off + i, 4u);
       }
       cp_async_commit();
     }
-    for (int kb = 0; kb < KB; ++kb) {
-      const uint32_t slot = ring + (uint32_t)(kb % kScaleAhead) * 256;
-      cp_async_wait<kScaleAhead - 1>();
-      float sa, sb;
-      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(sa), "=f"(sb) : "r"(slot) : "memory");
-      const float sc = sa * sb;
+    auto refill = [&](int kb, uint32_t so) {
       if (kb + kScaleAhead < KB) {
         const int kn = kb + kScaleAhead;
-        cp_async4(slot, g.A_scale + (size_t)kn * g.R + sa_row, sa_bytes);
-        cp_async4(slot + 4, g.W_scale + sb_off + kn, 4u);
+        cp_async4(sa_dst + so, g.A_scale + (size_t)kn * g.R + sa_row, sa_bytes);
+        cp_async4(sb_dst + so, g.W_scale + sb_off + kn, 4u);
       }
       cp_async_commit();
-      const uint32_t p = pit & 1u, pph = (pit >> 1) & 1u;
-      if (!mbar_wait(smem_u32(&sh->tfull[p]), pph, &sh->abort_flag, g.status, g.timeout_ns)) return;
+    };
+    // wait for partial p; hand the stage back (kReleaseStage)
+    auto take = [&](uint32_t p, uint32_t pph) -> bool {
+      if (!mbar_wait(smem_u32(&sh->tfull[p]), pph, &sh->abort_flag, g.status, g.timeout_ns)) return false;
       // the MMAs that read smem stage (pit % stages) are complete: hand the stage back to the TMA thread
       if (kReleaseStage && warp == kEpiWarp0 && lane == 0) mbar_arrive(smem_u32(&sh->empty[pit % kGemmStages]));
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + p * kGemmBN + h * 128;
-      acc.fold(taddr, sc);
+      return true;
+    };
+    // partial p is loaded: report it free
+    auto give_back = [&](uint32_t p) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -531,7 +569,61 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
         else
           mbar_arrive(smem_u32(&sh->tempty[p]));
       }
-      ++pit;
+    };
+    if (kSwap && swap) {
+      for (int kb = 0; kb < KB; ++kb) {
+        const uint32_t so = (uint32_t)(kb % kScaleAhead) * 256;
+        cp_async_wait<kScaleAhead - 1>();
+        __syncwarp();   // every lane's copy of this K-block's scales has landed
+        float sb;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sb) : "r"(sb_dst + so) : "memory");
+        // column scales, token 2i in the low half of c[i]
+        unsigned long long c[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float a0, a1, a2, a3;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                       : "r"(stg_s + so + i * 16)
+                       : "memory");
+          c[2 * i] = pack_f32x2(__fmul_rn(a0, sb), __fmul_rn(a1, sb));
+          c[2 * i + 1] = pack_f32x2(__fmul_rn(a2, sb), __fmul_rn(a3, sb));
+        }
+        __syncwarp();   // all lanes have read the slot before any lane refills it
+        refill(kb, so);
+        const uint32_t p = pit & 1u, pph = (pit >> 1) & 1u;
+        if (!take(p, pph)) return;
+        acc.fold_cols(tmem + ((uint32_t)(q * 32) << 16) + p * kGemmBN + h * kSwapRows, c);
+        give_back(p);
+        ++pit;
+      }
+    } else {
+      for (int kb = 0; kb < KB; ++kb) {
+        const uint32_t so = (uint32_t)(kb % kScaleAhead) * 256;
+        cp_async_wait<kScaleAhead - 1>();
+        float sa, sb;
+        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(sa), "=f"(sb) : "r"(sa_dst + so) : "memory");
+        const float sc = sa * sb;
+        refill(kb, so);
+        const uint32_t p = pit & 1u, pph = (pit >> 1) & 1u;
+        if (!take(p, pph)) return;
+        acc.fold(tmem + ((uint32_t)(q * 32) << 16) + p * kGemmBN + h * 128, sc);
+        give_back(p);
+        ++pit;
+      }
+    }
+    if (kSwap && swap) {
+      // Y^T column: this thread's output column, one bf16 per token (a warp
+      // store covers 32 consecutive columns of one row)
+      cp_async_wait<0>();
+      __syncwarp();
+      uint16_t* yc = g.Y + (size_t)row0 * g.N + (size_t)nb * kGemmBN + h * 128 + q * 32 + lane;
+#pragma unroll
+      for (int t = 0; t < kSwapRows; ++t) {
+        if (t < rows) yc[(size_t)t * g.N] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.col(t)));
+      }
+      if (kSignal && lane == 0) mbar_arrive(smem_u32(&sh->stored[slot]));
+      continue;
     }
     // bf16 output through the warp's staging tile: lane = row on the way in,
     // 8 lanes per row (4 rows per instruction) on the way out (the scale ring

@@ -16,6 +16,7 @@
 // bit-for-bit the same with half the FMA instructions.  Which one is faster
 // depends on the kernel around it (the standalone GEMM1: the packed form by
 // 4%; the fused stage1 kernel: the scalar form by 3%, measured on one box).
+// tmem_fold32x2 (at the end) folds the transposed units of few rows.
 #pragma once
 
 #include "common.cuh"
@@ -123,6 +124,24 @@ MOE_DEV void tmem_fold128x2(uint32_t taddr, float sc, unsigned long long (&acc)[
         "+l"(acc[48]), "+l"(acc[49]), "+l"(acc[50]), "+l"(acc[51]), "+l"(acc[52]), "+l"(acc[53]), "+l"(acc[54]), "+l"(acc[55]),
         "+l"(acc[56]), "+l"(acc[57]), "+l"(acc[58]), "+l"(acc[59]), "+l"(acc[60]), "+l"(acc[61]), "+l"(acc[62]), "+l"(acc[63])
       : "r"(taddr), "f"(sc)
+      : "memory");
+}
+
+// tmem_fold32x2: the transposed form.  acc[i] (i < 16, packed pairs as in
+// tmem_fold128x2) += 32 consecutive fp32 TMEM columns of this thread's lane
+// times a per-column scale, c[i] holding the scales of columns 2i and 2i+1.
+MOE_DEV void tmem_fold32x2(uint32_t taddr, const unsigned long long (&c)[16], unsigned long long (&acc)[64]) {
+  asm volatile(
+      "{\n\t.reg .b32 t<32>;\n\t.reg .b64 pt;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "mov.b64 pt, {t0, t1}; fma.rn.f32x2 %0, pt, %17, %0; mov.b64 pt, {t2, t3}; fma.rn.f32x2 %1, pt, %18, %1; mov.b64 pt, {t4, t5}; fma.rn.f32x2 %2, pt, %19, %2; mov.b64 pt, {t6, t7}; fma.rn.f32x2 %3, pt, %20, %3;\n\t"
+      "mov.b64 pt, {t8, t9}; fma.rn.f32x2 %4, pt, %21, %4; mov.b64 pt, {t10, t11}; fma.rn.f32x2 %5, pt, %22, %5; mov.b64 pt, {t12, t13}; fma.rn.f32x2 %6, pt, %23, %6; mov.b64 pt, {t14, t15}; fma.rn.f32x2 %7, pt, %24, %7;\n\t"
+      "mov.b64 pt, {t16, t17}; fma.rn.f32x2 %8, pt, %25, %8; mov.b64 pt, {t18, t19}; fma.rn.f32x2 %9, pt, %26, %9; mov.b64 pt, {t20, t21}; fma.rn.f32x2 %10, pt, %27, %10; mov.b64 pt, {t22, t23}; fma.rn.f32x2 %11, pt, %28, %11;\n\t"
+      "mov.b64 pt, {t24, t25}; fma.rn.f32x2 %12, pt, %29, %12; mov.b64 pt, {t26, t27}; fma.rn.f32x2 %13, pt, %30, %13; mov.b64 pt, {t28, t29}; fma.rn.f32x2 %14, pt, %31, %14; mov.b64 pt, {t30, t31}; fma.rn.f32x2 %15, pt, %32, %15;\n\t"
+      "}"
+      : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]), "+l"(acc[8]), "+l"(acc[9]), "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]), "+l"(acc[14]), "+l"(acc[15])
+      : "r"(taddr), "l"(c[0]), "l"(c[1]), "l"(c[2]), "l"(c[3]), "l"(c[4]), "l"(c[5]), "l"(c[6]), "l"(c[7]), "l"(c[8]), "l"(c[9]), "l"(c[10]), "l"(c[11]), "l"(c[12]), "l"(c[13]), "l"(c[14]), "l"(c[15])
       : "memory");
 }
 
