@@ -453,8 +453,8 @@ struct FoldAcc<false> {
   }
   MOE_DEV void fold(uint32_t taddr, float sc) { tmem_fold128(taddr, sc, v); }
   MOE_DEV uint32_t bf16x2(int c) const { return pack_bf16x2(v[c], v[c + 1]); }   // columns c, c + 1
-  // transposed units take the packed form only (epilogue_loop asserts it)
-  MOE_DEV void fold_cols(uint32_t, const unsigned long long (&)[16]) {}
+  // transposed unit: 32 token columns with their own scales into v[0..31]
+  MOE_DEV void fold_cols(uint32_t taddr, const unsigned long long (&c)[16]) { tmem_fold32(taddr, c, v); }
   MOE_DEV float col(int t) const { return v[t]; }
 };
 
@@ -488,7 +488,7 @@ struct FoldAcc<true> {
 template <bool kPacked, bool kSignal = false, bool kGather = false, bool kPair = false, bool kReleaseStage = false,
           bool kSwap = false>
 MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
-  static_assert(!kSwap || (kPacked && !kGather && !kPair), "transposed units: packed fold, dense A, one CTA");
+  static_assert(!kSwap || (!kGather && !kPair), "transposed units: dense A, one CTA");
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                 // TMEM lane quarter this warp may access
@@ -622,6 +622,7 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
       for (int t = 0; t < kSwapRows; ++t) {
         if (t < rows) yc[(size_t)t * g.N] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.col(t)));
       }
+      __syncwarp();
       if (kSignal && lane == 0) mbar_arrive(smem_u32(&sh->stored[slot]));
       continue;
     }

@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       drain_fills(S, it, g.timeout_ns);
     } else if (warp == 1) {
-      mma_loop<false>(S, KB, g.status, g.timeout_ns);
+      mma_loop<false, true>(S, KB, g.status, g.timeout_ns);
     } else if (warp == 2) {
       count_loop(S, g, c);
     } else {
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     regs_alloc<kRegsEpilogueC>();
-    epilogue_loop<true, true, false, false, true>(S, g);
+    epilogue_loop<true, true, false, false, true, true>(S, g);
     if (warp == kEpiWarp0 && lane == 0) {   // this CTA's GEMM work is done
       const unsigned long long now = globaltimer_ns();
       atomicMin(c.tr + MOE_GC_TRACE_GEMM_FIRST_DONE, now);

@@ -338,11 +338,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       drain_fills(S, it, p.g.timeout_ns);
     } else if (warp == 1) {
-      mma_loop<false>(S, KB, p.g.status, p.g.timeout_ns);
+      mma_loop<false, true>(S, KB, p.g.status, p.g.timeout_ns);
     }
   } else {
     regs_alloc<kRegsEpilogue>();
-    epilogue_loop<false, false, false, false, true>(S, p.g);
+    epilogue_loop<false, false, false, false, true, true>(S, p.g);
   }
   gemm_teardown(S);
   if (p.trace && threadIdx.x == 0) atomicMax(p.tr + MOE_TRACE_END, (unsigned long long)globaltimer_ns());

@@ -16,7 +16,8 @@
 // bit-for-bit the same with half the FMA instructions.  Which one is faster
 // depends on the kernel around it (the standalone GEMM1: the packed form by
 // 4%; the fused stage1 kernel: the scalar form by 3%, measured on one box).
-// tmem_fold32x2 (at the end) folds the transposed units of few rows.
+// tmem_fold32x2 and tmem_fold32 (at the end) fold the transposed units of few
+// rows, in the packed and the scalar form.
 #pragma once
 
 #include "common.cuh"
@@ -141,6 +142,23 @@ MOE_DEV void tmem_fold32x2(uint32_t taddr, const unsigned long long (&c)[16], un
       "mov.b64 pt, {t24, t25}; fma.rn.f32x2 %12, pt, %29, %12; mov.b64 pt, {t26, t27}; fma.rn.f32x2 %13, pt, %30, %13; mov.b64 pt, {t28, t29}; fma.rn.f32x2 %14, pt, %31, %14; mov.b64 pt, {t30, t31}; fma.rn.f32x2 %15, pt, %32, %15;\n\t"
       "}"
       : "+l"(acc[0]), "+l"(acc[1]), "+l"(acc[2]), "+l"(acc[3]), "+l"(acc[4]), "+l"(acc[5]), "+l"(acc[6]), "+l"(acc[7]), "+l"(acc[8]), "+l"(acc[9]), "+l"(acc[10]), "+l"(acc[11]), "+l"(acc[12]), "+l"(acc[13]), "+l"(acc[14]), "+l"(acc[15])
+      : "r"(taddr), "l"(c[0]), "l"(c[1]), "l"(c[2]), "l"(c[3]), "l"(c[4]), "l"(c[5]), "l"(c[6]), "l"(c[7]), "l"(c[8]), "l"(c[9]), "l"(c[10]), "l"(c[11]), "l"(c[12]), "l"(c[13]), "l"(c[14]), "l"(c[15])
+      : "memory");
+}
+
+// tmem_fold32: tmem_fold32x2 with scalar accumulators (acc[0..31], column t
+// in acc[t]) and fma.rn.f32; the same sums bit for bit.
+MOE_DEV void tmem_fold32(uint32_t taddr, const unsigned long long (&c)[16], float (&acc)[128]) {
+  asm volatile(
+      "{\n\t.reg .b32 t<32>;\n\t.reg .b32 cl, ch;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "mov.b64 {cl, ch}, %33; fma.rn.f32 %0, t0, cl, %0; fma.rn.f32 %1, t1, ch, %1; mov.b64 {cl, ch}, %34; fma.rn.f32 %2, t2, cl, %2; fma.rn.f32 %3, t3, ch, %3; mov.b64 {cl, ch}, %35; fma.rn.f32 %4, t4, cl, %4; fma.rn.f32 %5, t5, ch, %5; mov.b64 {cl, ch}, %36; fma.rn.f32 %6, t6, cl, %6; fma.rn.f32 %7, t7, ch, %7;\n\t"
+      "mov.b64 {cl, ch}, %37; fma.rn.f32 %8, t8, cl, %8; fma.rn.f32 %9, t9, ch, %9; mov.b64 {cl, ch}, %38; fma.rn.f32 %10, t10, cl, %10; fma.rn.f32 %11, t11, ch, %11; mov.b64 {cl, ch}, %39; fma.rn.f32 %12, t12, cl, %12; fma.rn.f32 %13, t13, ch, %13; mov.b64 {cl, ch}, %40; fma.rn.f32 %14, t14, cl, %14; fma.rn.f32 %15, t15, ch, %15;\n\t"
+      "mov.b64 {cl, ch}, %41; fma.rn.f32 %16, t16, cl, %16; fma.rn.f32 %17, t17, ch, %17; mov.b64 {cl, ch}, %42; fma.rn.f32 %18, t18, cl, %18; fma.rn.f32 %19, t19, ch, %19; mov.b64 {cl, ch}, %43; fma.rn.f32 %20, t20, cl, %20; fma.rn.f32 %21, t21, ch, %21; mov.b64 {cl, ch}, %44; fma.rn.f32 %22, t22, cl, %22; fma.rn.f32 %23, t23, ch, %23;\n\t"
+      "mov.b64 {cl, ch}, %45; fma.rn.f32 %24, t24, cl, %24; fma.rn.f32 %25, t25, ch, %25; mov.b64 {cl, ch}, %46; fma.rn.f32 %26, t26, cl, %26; fma.rn.f32 %27, t27, ch, %27; mov.b64 {cl, ch}, %47; fma.rn.f32 %28, t28, cl, %28; fma.rn.f32 %29, t29, ch, %29; mov.b64 {cl, ch}, %48; fma.rn.f32 %30, t30, cl, %30; fma.rn.f32 %31, t31, ch, %31;\n\t"
+      "}"
+      : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3]), "+f"(acc[4]), "+f"(acc[5]), "+f"(acc[6]), "+f"(acc[7]), "+f"(acc[8]), "+f"(acc[9]), "+f"(acc[10]), "+f"(acc[11]), "+f"(acc[12]), "+f"(acc[13]), "+f"(acc[14]), "+f"(acc[15]), "+f"(acc[16]), "+f"(acc[17]), "+f"(acc[18]), "+f"(acc[19]), "+f"(acc[20]), "+f"(acc[21]), "+f"(acc[22]), "+f"(acc[23]), "+f"(acc[24]), "+f"(acc[25]), "+f"(acc[26]), "+f"(acc[27]), "+f"(acc[28]), "+f"(acc[29]), "+f"(acc[30]), "+f"(acc[31])
       : "r"(taddr), "l"(c[0]), "l"(c[1]), "l"(c[2]), "l"(c[3]), "l"(c[4]), "l"(c[5]), "l"(c[6]), "l"(c[7]), "l"(c[8]), "l"(c[9]), "l"(c[10]), "l"(c[11]), "l"(c[12]), "l"(c[13]), "l"(c[14]), "l"(c[15])
       : "memory");
 }
