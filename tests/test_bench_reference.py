@@ -63,15 +63,20 @@ def test_sampler_times_every_nonempty_expert_once_before_repeating():
 
 
 def test_traffic_key_follows_kernel_code_not_comments(tmp_path, monkeypatch):
-    # the DRAM-traffic figure is keyed by a hash of the kernel sources' code:
-    # editing a comment keeps it, editing code drops it (null until recaptured)
+    # the DRAM-traffic figure is keyed by a hash of the dominant kernel's
+    # sources' code: editing a comment keeps it, editing code drops it (null
+    # until recaptured); code of other kernels does not enter
     import shutil
     src = os.path.join(ROOT, "combine_counting_sort_gb300", "csrc")
     fake_root = tmp_path / "root"
     shutil.copytree(src, fake_root / "combine_counting_sort_gb300" / "csrc")
     monkeypatch.setattr(bench, "ROOT", str(fake_root))
     h0 = bench.kernel_source_hash()
-    f = fake_root / "combine_counting_sort_gb300" / "csrc" / "stage1.cu"
+    csrc = fake_root / "combine_counting_sort_gb300" / "csrc"
+    other = csrc / "layout.cu"
+    other.write_text(other.read_text() + "\nstatic int unused_probe;\n")
+    assert bench.kernel_source_hash() == h0
+    f = csrc / "gemm1.cuh"
     text = f.read_text()
     f.write_text(text + "\n// a comment\n/* another\n comment */\n")
     assert bench.kernel_source_hash() == h0
