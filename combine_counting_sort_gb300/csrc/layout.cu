@@ -5,28 +5,30 @@
 // sort by (destination, first expert) so that a landed prefix of a run is a
 // prefix of experts; recv_layout commit: per-expert counts, padding of every
 // expert to the sort block, expert-major tables) as ONE launch: a cooperative
-// grid of at most one block per SM (T <= 32: a single block in a plain launch,
-// which needs neither barrier):
+// grid of at most 64 blocks, about 1024 pairs each (T <= 32: a single block
+// in a plain launch, which needs no barrier):
 //
-//   phase A  each block histograms its contiguous token range: experts of its
-//            pairs and first (smallest) experts of its tokens, with
-//            warp-aggregated shared-memory adds (__match_any_sync leaders);
-//            the block's ids and weights stay staged in shared memory.
-//   barrier  grid-wide barrier (bounded spin: MOE_ERR_TIMEOUT after 1 s).
-//   phase B  the per-block histograms are scanned down the blocks, one warp
-//            per expert column (in place: each entry becomes that block's
-//            exclusive prefix; the column total goes to a totals array);
-//            after a second grid barrier every block reads its own row of
-//            prefixes and the totals, scans across experts (expert offsets,
-//            tile offsets, first-expert offsets) in shared memory; block 0
-//            writes the E-sized tables; the tile tables and the rowmap are
-//            written one tile per warp over the whole grid.
-//   phase C  stable ranks: the block's pairs, in (token, slot) order, are cut
-//            into one contiguous slice per warp; per-warp histograms scanned
-//            across the warps give each warp its first row per expert, and each
-//            warp walks its slice 32 at a time (lanes with equal experts find
-//            each other with __match_any_sync and take consecutive rows); the
-//            token order by first expert is ranked the same way.
+//   phase A  each block counts its contiguous token range by both keys (the
+//            expert of each pair, the first (smallest) expert of each token):
+//            every warp histograms its own slice with warp-aggregated
+//            shared-memory adds (__match_any_sync leaders), and the slice
+//            histograms, scanned across the warps, become each warp's first
+//            position within the block; the block totals go to its row of a
+//            table in the workspace.  The block's ids and weights stay
+//            staged in shared memory.
+//   barrier  one grid-wide barrier (bounded spin: MOE_ERR_TIMEOUT after 1 s).
+//   phase B  every block reads the whole table (rows of 2E contiguous counts)
+//            and sums each column over the blocks before it (its first row
+//            per expert within the expert) and over all blocks (the totals);
+//            one scan across experts gives expert offsets, tile offsets and
+//            first-expert offsets; block 0 writes the E-sized tables; the
+//            tile tables and the rowmap are written one tile per warp over
+//            the whole grid.
+//   phase C  stable ranks: each warp walks its slice 32 keys at a time
+//            (lanes with equal keys find each other with __match_any_sync
+//            and take consecutive rows in lane order), the token order by
+//            first expert the same way.  A block whose range exceeds one
+//            staged chunk stages, histograms and ranks chunk by chunk.
 //
 // Logical group g holds experts [g*E/G, (g+1)*E/G) (the Mojo EPDispatchKernel
 // page's n_local_experts = n_experts / n_ranks), so the key (group, expert)
@@ -37,18 +39,26 @@
 namespace moe {
 
 constexpr int kLayoutThreads = 512;
-constexpr int kLayoutMaxBlocks = 256;     // bound of the workspace's per-block histograms
+constexpr int kLayoutGridCap = 64;        // blocks of one grid at most (each reads every block's row)
+constexpr int kLayoutPairsPerBlock = 1024;
 constexpr int kChunkPairs = 4096;         // pairs staged in shared memory per pass
 constexpr int kLayoutWarps = kLayoutThreads / 32;
+constexpr int kStageRounds = kChunkPairs / kLayoutThreads;   // staged pairs per thread
+// phase B's partial column sums: 2 x (row groups x row stride) <= 2 x 4 x kLayoutThreads ints
+constexpr int kPartInts = 8 * kLayoutThreads;
+static_assert(kPartInts % 4 == 0, "the arrays after it stay 16-byte aligned at their start");
+static_assert(kChunkPairs % kLayoutThreads == 0, "whole staging rounds");
+
+// Row stride (ints) of the workspace table of per-block counts: 2E rounded up
+// to whole 16-byte vectors.
+__host__ __device__ __forceinline__ int layout_row_stride(int E) { return (2 * E + 3) & ~3; }
 
 struct LayoutArgs {
   const int32_t* ids;
   const float* w;
   LayoutDev L;
-  int32_t* ws_hist;     // [E][kLayoutMaxBlocks]: expert e's count in block b at e * kLayoutMaxBlocks + b
-  int32_t* ws_fhist;    // [E][kLayoutMaxBlocks]
-  int32_t* ws_tot;      // [2][E] column totals of ws_hist / ws_fhist
-  uint32_t* ws_barrier; // [2] zeroed in-stream before the launch
+  int32_t* ws_tab;      // [nblk][2E]: block b's expert counts, then its first-expert counts
+  uint32_t* ws_barrier; // [1] zeroed in-stream before the launch
   int32_t* status;
   int tpb;              // tokens per block
   uint64_t timeout_ns;
@@ -91,37 +101,6 @@ __device__ bool grid_barrier(uint32_t* ctr, int nblk, int32_t* status, uint64_t 
   return *flag == 0;
 }
 
-// One warp scans column `col` (nblk <= 256 contiguous entries) in place into
-// exclusive prefixes and returns the column total (all lanes).  Rows of 32
-// entries, one coalesced load per row: each row's warp scan on top of the
-// rows before it.
-__device__ int warp_column_scan(int32_t* col, int nblk) {
-  const int lane = threadIdx.x & 31;
-  const int rows = (nblk + 31) / 32;     // <= 8
-  int v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int bb = i * 32 + lane;
-    v[i] = (i < rows && bb < nblk) ? __ldcg(col + bb) : 0;
-  }
-  int base = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (i < rows) {
-      int incl = v[i];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      const int bb = i * 32 + lane;
-      if (bb < nblk) col[bb] = base + incl - v[i];
-      base += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
-  return base;
-}
-
 // Exclusive scan over n <= 2*blockDim values held in shared memory (in place),
 // returning the total.  `scratch` holds >= 32 ints.
 __device__ int block_exclusive_scan(int* data, int n, int* scratch) {
@@ -158,106 +137,258 @@ __device__ int block_exclusive_scan(int* data, int n, int* scratch) {
   return total;
 }
 
+// Exclusive scans, in place, of three arrays of n <= 2*blockDim values held in
+// shared memory, in one pass; tot[i] receives array i's total.  `scratch`
+// holds >= 3 * 32 + 3 ints.
+__device__ void block_exclusive_scan3(int* d0, int* d1, int* d2, int n, int* scratch, int* tot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = blockDim.x >> 5;
+  int* d[3] = {d0, d1, d2};
+  int a[3], v[3], incl[3];
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    a[i] = (2 * tid < n) ? d[i][2 * tid] : 0;
+    v[i] = a[i] + ((2 * tid + 1 < n) ? d[i][2 * tid + 1] : 0);
+    incl[i] = v[i];
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int u = __shfl_up_sync(0xffffffffu, incl[i], o);
+      if (lane >= o) incl[i] += u;
+    }
+  }
+  if (lane == 31) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) scratch[i * 32 + warp] = incl[i];
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int w = lane < nw ? scratch[i * 32 + lane] : 0;
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += u;
+      }
+      if (lane < nw) scratch[i * 32 + lane] = wi - w;   // exclusive warp offsets
+      if (lane == 31) scratch[96 + i] = wi;            // total
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const int excl = scratch[i * 32 + warp] + incl[i] - v[i];
+    if (2 * tid < n) d[i][2 * tid] = excl;
+    if (2 * tid + 1 < n) d[i][2 * tid + 1] = excl + a[i];
+    tot[i] = scratch[96 + i];
+  }
+  __syncthreads();
+}
+
+// Slice of the block's keys ranked by warp `warp`: a contiguous run of whole
+// 32-key rounds, one run per warp, in key order.
+__device__ __forceinline__ void warp_slice(int n, int warp, int& s0, int& s1) {
+  const int per = (((n + kLayoutWarps - 1) / kLayoutWarps) + 31) & ~31;
+  s0 = min(n, warp * per);
+  s1 = min(n, s0 + per);
+}
+
 __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs a) {
-  extern __shared__ int smem_i[];
+  extern __shared__ __align__(16) int smem_i[];
   const int E = a.L.E, k = a.L.k, T = a.L.T, BM = a.L.block_m;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x, nblk = gridDim.x;
 
-  int* hist = smem_i;             // [E]   block histogram, later the running row cursor
-  int* fhist = hist + E;          // [E]   block first-expert histogram, later the token cursor
+  int* part = smem_i;             // [kPartInts] phase B column sums (first: 16-byte aligned, int4 stores)
+  int* hist = part + kPartInts;   // [E]   block histogram, later the block's first row per expert
+  int* fhist = hist + E;          // [E]   block first-expert histogram, later the block's first position
   int* eoff = fhist + E;          // [E+1] expert offsets
   int* toff = eoff + E + 1;       // [E+1] expert tile offsets
   int* foff = toff + E + 1;       // [E+1] first-expert offsets
-  int* scratch = foff + E + 1;    // [64]
-  int* s_ids = scratch + 64;      // [kChunkPairs]
-  float* s_w = reinterpret_cast<float*>(s_ids + kChunkPairs);  // [kChunkPairs]
+  int* scratch = foff + E + 1;    // [128]
+  int* s_ids = scratch + 128;     // [kChunkPairs]
+  float* s_w = reinterpret_cast<float*>(s_ids + kChunkPairs);   // [kChunkPairs]
+  int* whist = reinterpret_cast<int*>(s_w + kChunkPairs);       // [2][kLayoutWarps][E]
 
   const int t0 = min(T, b * a.tpb), t1 = min(T, t0 + a.tpb);
   const int chunk_tokens = max(1, kChunkPairs / k);
   const bool one_chunk = (t1 - t0) <= chunk_tokens;
 
+  // key of item i of a staged chunk: pass 0 the expert of pair i, pass 1 the
+  // first (smallest) expert of token i; -1 for an invalid id
+  auto key_of = [&](int pass, int i) -> int {
+    if (pass == 0) {
+      const int e = s_ids[i];
+      return (e < 0 || e >= E) ? -1 : e;
+    }
+    const int fe = first_expert(s_ids + i * k, k, E);
+    return fe >= E ? -1 : fe;
+  };
+  // stage pairs [q0, q1) (at most kChunkPairs): every load issued before the
+  // first store, so the chunk costs one memory round trip
+  auto stage = [&](int q0, int q1) {
+    int vi[kStageRounds];
+    float vw[kStageRounds];
+#pragma unroll
+    for (int j = 0; j < kStageRounds; ++j) {
+      const int p = q0 + tid + j * kLayoutThreads;
+      if (p < q1) {
+        vi[j] = __ldg(a.ids + p);
+        vw[j] = __ldg(a.w + p);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kStageRounds; ++j) {
+      const int p = q0 + tid + j * kLayoutThreads;
+      if (p < q1) {
+        s_ids[p - q0] = vi[j];
+        s_w[p - q0] = vw[j];
+      }
+    }
+  };
+
   for (int e = tid; e < E; e += blockDim.x) { hist[e] = 0; fhist[e] = 0; }
+  if (one_chunk)
+    for (int i = tid; i < 2 * kLayoutWarps * E; i += blockDim.x) whist[i] = 0;
   __syncthreads();
 
   // ---------------- phase A: block histograms
-  for (int c0 = t0; c0 < t1; c0 += chunk_tokens) {
-    const int c1 = min(t1, c0 + chunk_tokens);
-    const int q0 = c0 * k, q1 = c1 * k;
-    for (int p = q0 + tid; p < q1; p += blockDim.x) {
-      s_ids[p - q0] = a.ids[p];
-      s_w[p - q0] = a.w[p];
+  if (one_chunk) {
+    // One chunk (every grid this library launches up to T*k = 64 * 4096
+    // pairs): per-warp slice histograms of both keys, kept for phase C, then
+    // scanned across the warps in place (each entry becomes the warp's first
+    // position within the block) with the block totals left in hist / fhist.
+    const int q0 = t0 * k, q1 = t1 * k;
+    stage(q0, q1);
+    __syncthreads();
+    for (int i = q0 + tid; i < q1; i += blockDim.x) {
+      const int e = s_ids[i - q0];
+      if (e >= E || (e < 0 && !a.quiet)) set_status(a.status, MOE_ERR_EXPERT_ID);
+    }
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      int s0, s1;
+      warp_slice(pass == 0 ? q1 - q0 : t1 - t0, warp, s0, s1);
+      int* wh = whist + (pass * kLayoutWarps + warp) * E;
+      for (int base = s0; base < s1; base += 32) {
+        const int i = base + lane;
+        const int e = i < s1 ? key_of(pass, i) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) wh[e] += __popc(peers);
+        __syncwarp();
+      }
     }
     __syncthreads();
-    for (int base = q0; base < q1; base += blockDim.x) {
-      const int p = base + tid;
-      int e = -1;
-      if (p < q1) {
-        e = s_ids[p - q0];
-        if (e < 0 || e >= E) {
-          if (!(a.quiet && e < 0)) set_status(a.status, MOE_ERR_EXPERT_ID);
-          e = -1;
+    for (int c = tid; c < 2 * E; c += blockDim.x) {
+      int* col = whist + (c < E ? 0 : kLayoutWarps * E) + (c % E);
+      int v[kLayoutWarps];
+#pragma unroll
+      for (int w2 = 0; w2 < kLayoutWarps; ++w2) v[w2] = col[w2 * E];
+      int run = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < kLayoutWarps; ++w2) {
+        col[w2 * E] = run;
+        run += v[w2];
+      }
+      (c < E ? hist : fhist)[c % E] = run;
+    }
+  } else {
+    for (int c0 = t0; c0 < t1; c0 += chunk_tokens) {
+      const int c1 = min(t1, c0 + chunk_tokens);
+      const int q0 = c0 * k, q1 = c1 * k;
+      stage(q0, q1);
+      __syncthreads();
+      for (int base = q0; base < q1; base += blockDim.x) {
+        const int p = base + tid;
+        int e = -1;
+        if (p < q1) {
+          e = s_ids[p - q0];
+          if (e < 0 || e >= E) {
+            if (!(a.quiet && e < 0)) set_status(a.status, MOE_ERR_EXPERT_ID);
+            e = -1;
+          }
         }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[e], __popc(peers));
       }
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[e], __popc(peers));
-    }
-    for (int base = c0; base < c1; base += blockDim.x) {
-      const int t = base + tid;
-      int fe = -1;
-      if (t < c1) {
-        fe = first_expert(s_ids + (t - c0) * k, k, E);
-        if (fe >= E) fe = -1;
+      for (int base = c0; base < c1; base += blockDim.x) {
+        const int t = base + tid;
+        const int fe = t < c1 ? key_of(1, t - c0) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, fe);
+        if (fe >= 0 && lane == __ffs(peers) - 1) atomicAdd(&fhist[fe], __popc(peers));
       }
-      const unsigned peers = __match_any_sync(0xffffffffu, fe);
-      if (fe >= 0 && lane == __ffs(peers) - 1) atomicAdd(&fhist[fe], __popc(peers));
+      __syncthreads();
     }
-    __syncthreads();
   }
+  __syncthreads();
+
+  // ---------------- phase B: every block's prefixes and the totals
   if (nblk == 1) {
     // one block (small batches, a plain launch): its histograms are the totals
     // and its prefixes are zero; no workspace, no grid barrier
     for (int e = tid; e < E; e += blockDim.x) {
-      const int tot = hist[e], ftot = fhist[e];
+      eoff[e] = hist[e];
+      toff[e] = (hist[e] + BM - 1) / BM;
+      foff[e] = fhist[e];
       hist[e] = 0;
       fhist[e] = 0;
-      eoff[e] = tot;
-      toff[e] = (tot + BM - 1) / BM;
-      foff[e] = ftot;
     }
   } else {
-    for (int e = tid; e < E; e += blockDim.x) {
-      a.ws_hist[(size_t)e * kLayoutMaxBlocks + b] = hist[e];
-      a.ws_fhist[(size_t)e * kLayoutMaxBlocks + b] = fhist[e];
-    }
-
-    // ---------------- phase B1: scan every expert column down the blocks (one warp per column)
-    if (!grid_barrier(a.ws_barrier, nblk, a.status, a.timeout_ns, &scratch[63])) return;
-    {
-      const int nwarps = blockDim.x >> 5;
-      for (int item = b * nwarps + warp; item < 2 * E; item += nblk * nwarps) {
-        int32_t* col = (item < E ? a.ws_hist : a.ws_fhist) + (size_t)(item % E) * kLayoutMaxBlocks;
-        const int total = warp_column_scan(col, nblk);
-        if (lane == 0) a.ws_tot[item] = total;
+    // this block's row of the table [nblk][RS] (expert counts, then
+    // first-expert counts, padded to 16-byte vectors)
+    const int RS = layout_row_stride(E);
+    int32_t* row = a.ws_tab + (size_t)b * RS;
+    for (int c = tid; c < RS; c += blockDim.x) row[c] = c < 2 * E ? (c < E ? hist : fhist)[c % E] : 0;
+    if (!grid_barrier(a.ws_barrier, nblk, a.status, a.timeout_ns, &scratch[127])) return;
+    // every block reads the whole table: each thread one 16-byte vector of
+    // columns in a group of rows, 16 rows in flight at a time; the column sums
+    // over the blocks before this one and over all blocks meet in shared
+    // memory (part: [2][ngroups][RS], prefixes then totals)
+    const int nvec = RS / 4;
+    const int ngroups = max(1, kLayoutThreads / nvec);
+    for (int i = tid; i < 2 * ngroups * RS; i += blockDim.x) part[i] = 0;
+    __syncthreads();
+    for (int vt = tid; vt < nvec * ngroups; vt += blockDim.x) {
+      const int vc = vt % nvec, g = vt / nvec;
+      int4 pre = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
+      for (int r0 = g; r0 < nblk; r0 += 16 * ngroups) {
+        int4 v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = r0 + i * ngroups;
+          v[i] = r < nblk ? __ldcg(reinterpret_cast<const int4*>(a.ws_tab + (size_t)r * RS) + vc)
+                          : make_int4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = r0 + i * ngroups;
+          tot.x += v[i].x; tot.y += v[i].y; tot.z += v[i].z; tot.w += v[i].w;
+          if (r < b) { pre.x += v[i].x; pre.y += v[i].y; pre.z += v[i].z; pre.w += v[i].w; }
+        }
       }
+      reinterpret_cast<int4*>(part + g * RS)[vc] = pre;
+      reinterpret_cast<int4*>(part + (ngroups + g) * RS)[vc] = tot;
     }
-    if (!grid_barrier(a.ws_barrier + 1, nblk, a.status, a.timeout_ns, &scratch[63])) return;
-
-    // ---------------- phase B2: this block's prefixes, expert scans
-    for (int e = tid; e < E; e += blockDim.x) {
-      const int tot = __ldcg(a.ws_tot + e), ftot = __ldcg(a.ws_tot + E + e);
-      hist[e] = __ldcg(a.ws_hist + (size_t)e * kLayoutMaxBlocks + b);     // this block's first row within expert e (relative)
-      fhist[e] = __ldcg(a.ws_fhist + (size_t)e * kLayoutMaxBlocks + b);   // this block's first position within first-expert e
-      eoff[e] = tot;
-      toff[e] = (tot + BM - 1) / BM;
-      foff[e] = ftot;
+    __syncthreads();
+    for (int c = tid; c < 2 * E; c += blockDim.x) {
+      int pre = 0, tot = 0;
+      for (int g = 0; g < ngroups; ++g) {
+        pre += part[g * RS + c];
+        tot += part[(ngroups + g) * RS + c];
+      }
+      if (c < E) { hist[c] = pre; eoff[c] = tot; toff[c] = (tot + BM - 1) / BM; }
+      else { fhist[c - E] = pre; foff[c - E] = tot; }
     }
   }
   __syncthreads();
-  const int total_rows = block_exclusive_scan(eoff, E, scratch);
-  const int total_tiles = block_exclusive_scan(toff, E, scratch);
-  const int total_first = block_exclusive_scan(foff, E, scratch);
-  if (tid == 0) { eoff[E] = total_rows; toff[E] = total_tiles; foff[E] = total_first; }
+  int tot3[3];
+  block_exclusive_scan3(eoff, toff, foff, E, scratch, tot3);
+  const int total_tiles = tot3[1];
+  if (tid == 0) { eoff[E] = tot3[0]; toff[E] = tot3[1]; foff[E] = tot3[2]; }
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x) {
     hist[e] += eoff[e];
@@ -278,10 +409,9 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
   }
   // tile tables and rowmap: one warp per tile, grid-stride over all blocks'
   // warps; one search for the tile's expert, then the tile's BM rowmap slots
-  // in coalesced runs of 32 (per-slot searches cost ~1 us more per call)
+  // in coalesced runs of 32
   {
-    const int nwarps = blockDim.x >> 5;
-    const int gw = b * nwarps + warp, gwstride = nblk * nwarps;
+    const int gw = b * kLayoutWarps + warp, gwstride = nblk * kLayoutWarps;
     const int cap = a.L.max_tiles;
     for (int m = gw; m < cap; m += gwstride) {
       int e = -1, begin = T * k, rows = 0;
@@ -307,81 +437,78 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
   __syncthreads();
 
   // ---------------- phase C: stable ranks within the block, all warps
-  // Each chunk's pairs (then its tokens) are cut into one contiguous slice per
-  // warp.  A per-warp histogram of the slice, scanned across the warps on top
-  // of the block's running cursors, gives every warp its first row per
-  // expert; each warp then ranks its slice 32 at a time (lanes with equal
-  // keys find each other with __match_any_sync and take consecutive rows in
-  // lane order), which keeps the (token, slot) order stable.
-  int* whist = reinterpret_cast<int*>(s_w + kChunkPairs);   // [kLayoutWarps][E]
-  int* wh = whist + warp * E;
+  // Each warp walks its slice 32 keys at a time: lanes with equal keys find
+  // each other with __match_any_sync and take consecutive positions in lane
+  // order after the warp's running first position for that key, which keeps
+  // the (token, slot) order stable.  One chunk: the slice histograms of phase
+  // A, scanned, are the warps' first positions within the block.  More
+  // chunks: each chunk is staged again, histogrammed per warp and scanned on
+  // top of the block's running cursors.
+  auto rank = [&](int pass, int q0, int c0, int n, int* cursor_base, int* wh) {
+    int s0, s1;
+    warp_slice(n, warp, s0, s1);
+    for (int base = s0; base < s1; base += 32) {
+      const int i = base + lane;
+      const int e = i < s1 ? key_of(pass, i) : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int pos = e >= 0 ? cursor_base[e] + wh[e] + __popc(peers & lanemask_lt()) : -1;
+      if (pass == 0) {
+        if (i < s1) {
+          const int p = q0 + i;
+          a.L.pair_row[p] = pos;
+          if (e >= 0) {
+            a.L.row_pair[pos] = p;
+            a.L.row_weight[pos] = s_w[i];
+          }
+        }
+      } else if (e >= 0) {
+        a.L.token_order[pos] = c0 + i;
+      }
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) wh[e] += __popc(peers);
+      __syncwarp();
+    }
+  };
+  if (one_chunk) {
+    rank(0, t0 * k, t0, (t1 - t0) * k, hist, whist + warp * E);
+    rank(1, t0 * k, t0, t1 - t0, fhist, whist + (kLayoutWarps + warp) * E);
+    return;
+  }
   for (int c0 = t0; c0 < t1; c0 += chunk_tokens) {
     const int c1 = min(t1, c0 + chunk_tokens);
     const int q0 = c0 * k, q1 = c1 * k;
-    if (!one_chunk) {
-      __syncthreads();
-      for (int p = q0 + tid; p < q1; p += blockDim.x) {
-        s_ids[p - q0] = a.ids[p];
-        s_w[p - q0] = a.w[p];
-      }
-      __syncthreads();
-    }
+    __syncthreads();
+    stage(q0, q1);
+    __syncthreads();
     for (int pass = 0; pass < 2; ++pass) {
-      // pass 0: pairs [q0, q1) keyed by expert; pass 1: tokens [c0, c1) keyed by first expert
       const int n = pass == 0 ? q1 - q0 : c1 - c0;
       int* cursor = pass == 0 ? hist : fhist;
-      const int per = (((n + kLayoutWarps - 1) / kLayoutWarps) + 31) & ~31;
-      const int s0 = min(n, warp * per), s1 = min(n, s0 + per);
-      auto key_of = [&](int i) -> int {   // i < n; -1 for an invalid expert id
-        if (pass == 0) {
-          const int e = s_ids[i];
-          return (e < 0 || e >= E) ? -1 : e;
-        }
-        const int fe = first_expert(s_ids + i * k, k, E);
-        return fe >= E ? -1 : fe;
-      };
+      int* wh = whist + warp * E;
       for (int i = tid; i < kLayoutWarps * E; i += blockDim.x) whist[i] = 0;
       __syncthreads();
+      int s0, s1;
+      warp_slice(n, warp, s0, s1);
       for (int base = s0; base < s1; base += 32) {
         const int i = base + lane;
-        const int e = i < s1 ? key_of(i) : -1;
+        const int e = i < s1 ? key_of(pass, i) : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         if (e >= 0 && lane == __ffs(peers) - 1) wh[e] += __popc(peers);
         __syncwarp();
       }
       __syncthreads();
       for (int e = tid; e < E; e += blockDim.x) {
-        int run = cursor[e];
+        int run = 0;
         for (int w2 = 0; w2 < kLayoutWarps; ++w2) {
           const int c = whist[w2 * E + e];
           whist[w2 * E + e] = run;
           run += c;
         }
-        cursor[e] = run;
+        whist[kLayoutWarps * E + e] = run;   // this chunk's count of key e
       }
       __syncthreads();
-      for (int base = s0; base < s1; base += 32) {
-        const int i = base + lane;
-        const int e = i < s1 ? key_of(i) : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int pos = e >= 0 ? wh[e] + __popc(peers & lanemask_lt()) : -1;
-        if (pass == 0) {
-          if (i < s1) {
-            const int p = q0 + i;
-            a.L.pair_row[p] = pos;
-            if (e >= 0) {
-              a.L.row_pair[pos] = p;
-              a.L.row_weight[pos] = s_w[i];
-            }
-          }
-        } else if (e >= 0) {
-          a.L.token_order[pos] = c0 + i;
-        }
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) wh[e] += __popc(peers);
-        __syncwarp();
-      }
-      __syncthreads();   // whist is cleared for the next pass
+      rank(pass, q0, c0, n, cursor, wh);
+      __syncthreads();
+      for (int e = tid; e < E; e += blockDim.x) cursor[e] += whist[kLayoutWarps * E + e];
     }
   }
 }
@@ -443,12 +570,12 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 using namespace moe;
 
 static size_t layout_smem_bytes(int E) {
-  return sizeof(int) * (size_t)(2 * E + 3 * (E + 1) + 64 + kChunkPairs) + sizeof(float) * kChunkPairs +
-         sizeof(int) * (size_t)kLayoutWarps * E;
+  return sizeof(int) * (size_t)(2 * E + 3 * (E + 1) + 128 + kChunkPairs) + sizeof(float) * kChunkPairs +
+         sizeof(int) * (size_t)2 * kLayoutWarps * E + sizeof(int) * (size_t)kPartInts;
 }
 
 size_t moe_layout_ws_bytes(int E) {
-  return 256 + 2 * sizeof(int32_t) * (size_t)kLayoutMaxBlocks * E + 2 * sizeof(int32_t) * (size_t)E;
+  return 256 + sizeof(int32_t) * (size_t)kLayoutGridCap * layout_row_stride(E);
 }
 
 // Grid, workspace pointers and launch shared by both entry points.  `ws` is
@@ -466,15 +593,19 @@ int launch_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_layout_kernel, kLayoutThreads, smem) != cudaSuccess || per_sm < 1)
     return MOE_ERR_CUDA;
-  // One block per SM at most, ~32 tokens per block.  The tile tables and the
-  // rowmap (max_tiles x 128 slots, most of them -1 on small batches) are
-  // written one tile per warp over the whole grid, and one SM writes them
-  // slowly, so a grid of more than one block has at least one warp per tile
-  // (blocks past the last token have empty ranges).  A single block (T <= 32)
-  // runs as a plain launch with no workspace memset and no grid barrier.
-  int nblk = (L->T + 31) / 32;
-  if (nblk > 1) nblk = std::max(nblk, (L->max_tiles + kLayoutWarps - 1) / kLayoutWarps);
-  nblk = std::min(nblk, std::min(nsm * per_sm, std::min(nsm, kLayoutMaxBlocks)));
+  // About kLayoutPairsPerBlock pairs per block, at most kLayoutGridCap
+  // blocks (every block reads every block's row of counts after the barrier,
+  // so the grid stays small) and one per SM.  The tile tables and the rowmap
+  // (max_tiles x 128 slots, most of them -1 on small batches) are written one
+  // tile per warp over the whole grid, so a grid of more than one block has
+  // at least one warp per two tiles (blocks past the last token have empty
+  // ranges).  A single block (T <= 32) runs as a plain launch with no
+  // workspace memset and no grid barrier.
+  const long long pairs = (long long)L->T * L->k;
+  int nblk = L->T <= 32 ? 1 : (int)std::min<long long>((pairs + kLayoutPairsPerBlock - 1) / kLayoutPairsPerBlock,
+                                                        kLayoutGridCap);
+  if (L->T > 32) nblk = std::max(nblk, std::min(kLayoutGridCap, (L->max_tiles + 2 * kLayoutWarps - 1) / (2 * kLayoutWarps)));
+  nblk = std::min(nblk, std::min(nsm * per_sm, std::min(nsm, kLayoutGridCap)));
   nblk = std::max(nblk, 1);
   const int tpb = (L->T + nblk - 1) / nblk;
 
@@ -483,9 +614,7 @@ int launch_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout
   a.w = topk_w;
   a.L = to_dev(L);
   a.ws_barrier = reinterpret_cast<uint32_t*>(ws);
-  a.ws_hist = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + 256);
-  a.ws_fhist = a.ws_hist + (size_t)kLayoutMaxBlocks * L->E;
-  a.ws_tot = a.ws_fhist + (size_t)kLayoutMaxBlocks * L->E;
+  a.ws_tab = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + 256);
   a.status = status;
   a.tpb = tpb;
   a.timeout_ns = 1000000000ull;
@@ -544,7 +673,7 @@ extern "C" int moe_router_topk(const float* logits, int T, int E, int k, int32_t
 // callers that cannot allocate device memory: a plugin inside a framework
 // whose memory pool owns the whole device, a latency-critical path that must
 // not pay the device-wide synchronisation a cudaMalloc can cause, or a
-// deployment that sizes all memory once at load time.  The array (514 KiB +
+// deployment that sizes all memory once at load time.  The array (128 KiB +
 // 256 B, for up to 256 experts) is reserved on every GPU that loads the
 // library and stays there until the process exits.  The first call on a
 // device looks its address up (make that call outside any stream capture);
@@ -552,10 +681,9 @@ extern "C" int moe_router_topk(const float* logits, int T, int E, int k, int32_t
 
 namespace moe {
 constexpr int kNoAllocMaxExperts = MOE_NOALLOC_MAX_EXPERTS;
-// header (grid-barrier counters) + two per-block histograms of up to kLayoutMaxBlocks x 256
-// experts + their column totals
-constexpr size_t kNoAllocScratchBytes = 256 + 2 * sizeof(int32_t) * (size_t)kLayoutMaxBlocks * kNoAllocMaxExperts +
-                                        2 * sizeof(int32_t) * (size_t)kNoAllocMaxExperts;
+// header (grid-barrier counter) + one row of 2 x 256 counts per block of the grid
+constexpr size_t kNoAllocScratchBytes = 256 + sizeof(int32_t) * (size_t)kLayoutGridCap * 2 * kNoAllocMaxExperts;
+static_assert(2 * kNoAllocMaxExperts % 4 == 0, "whole 16-byte rows");
 }  // namespace moe
 
 static __device__ __align__(256) unsigned char g_layout_scratch[moe::kNoAllocScratchBytes];

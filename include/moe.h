@@ -121,10 +121,10 @@ typedef struct moe_layout {
  *   topk_w    device f32 [T, k] router weights (copied to row_weight).
  *   ws        device workspace of at least layout_ws_bytes (contents ignored;
  *             the call initialises what it uses, in-stream).
- * One launch: a cooperative grid of at most one block per SM with two
- * grid-wide barriers (each bounded: a barrier not reached within 1 s writes
+ * One launch: a cooperative grid of at most 64 blocks (one per SM) with one
+ * grid-wide barrier (bounded: a barrier not reached within 1 s writes
  * MOE_ERR_TIMEOUT to *status and the kernel returns), or, for T <= 32, a
- * single block in a plain launch with neither. */
+ * single block in a plain launch without it. */
 int moe_route_layout(const int32_t* topk_ids, const float* topk_w, const moe_layout_t* L,
                      void* ws, size_t ws_bytes, int32_t* status, moe_stream_t stream);
 
@@ -138,7 +138,7 @@ int moe_route_layout(const int32_t* topk_ids, const float* topk_w, const moe_lay
  * counterpart of this entry point.
  *   Limit: E <= MOE_NOALLOC_MAX_EXPERTS (larger E returns MOE_ERR_UNSUPPORTED);
  *   other limits and outputs as moe_route_layout.
- *   The array (about 512 KiB) is reserved on every GPU that loads the library
+ *   The array (about 128 KiB) is reserved on every GPU that loads the library
  *   until the process exits.  Every call made outside a stream capture looks
  *   up the array's device address (so a context reset is followed); a call
  *   inside a capture reuses the address of the last uncaptured call on that
