@@ -251,6 +251,19 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
     }
   };
 
+  // one chunk: its loads are in flight while the histograms are cleared
+  int vi[kStageRounds];
+  float vw[kStageRounds];
+  if (one_chunk) {
+#pragma unroll
+    for (int j = 0; j < kStageRounds; ++j) {
+      const int p = t0 * k + tid + j * kLayoutThreads;
+      if (p < t1 * k) {
+        vi[j] = __ldg(a.ids + p);
+        vw[j] = __ldg(a.w + p);
+      }
+    }
+  }
   for (int e = tid; e < E; e += blockDim.x) { hist[e] = 0; fhist[e] = 0; }
   if (one_chunk)
     for (int i = tid; i < 2 * kLayoutWarps * E; i += blockDim.x) whist[i] = 0;
@@ -263,7 +276,14 @@ __global__ void __launch_bounds__(kLayoutThreads) route_layout_kernel(LayoutArgs
     // scanned across the warps in place (each entry becomes the warp's first
     // position within the block) with the block totals left in hist / fhist.
     const int q0 = t0 * k, q1 = t1 * k;
-    stage(q0, q1);
+#pragma unroll
+    for (int j = 0; j < kStageRounds; ++j) {
+      const int p = q0 + tid + j * kLayoutThreads;
+      if (p < q1) {
+        s_ids[p - q0] = vi[j];
+        s_w[p - q0] = vw[j];
+      }
+    }
     __syncthreads();
     for (int i = q0 + tid; i < q1; i += blockDim.x) {
       const int e = s_ids[i - q0];
