@@ -77,6 +77,57 @@ def test_layout_invalid_expert_id_is_reported():
     assert sorted(pr[valid]) == [0, 1, 2, 3]
 
 
+def layout_of_valid_pairs(ids, w, E, G):
+    """The layout of the pairs with an id in [0, E), the others skipped: the
+    oracle's definition (stable counting sort by (group, expert)) restricted
+    to the valid pairs, each token's first expert taken over its valid ids."""
+    T, k = ids.shape
+    flat = ids.reshape(-1).astype(np.int64)
+    ok = (flat >= 0) & (flat < E)
+    epg = E // G
+    p_valid = np.nonzero(ok)[0]
+    key = (flat[p_valid] // epg) * E + flat[p_valid]
+    row_pair = p_valid[np.argsort(key, kind="stable")]
+    pair_row = np.full(T * k, -1, np.int64)
+    pair_row[row_pair] = np.arange(len(row_pair))
+    count = np.bincount(flat[ok], minlength=E)
+    masked = np.where(ok.reshape(T, k), ids, E)
+    first = masked.min(axis=1)
+    has = first < E
+    tok = np.nonzero(has)[0]
+    token_order = tok[np.argsort(first[has], kind="stable")]
+    return dict(pair_row=pair_row, row_pair=row_pair, row_weight=w.reshape(-1)[row_pair], count=count,
+                expert_offset=np.concatenate([[0], np.cumsum(count)]),
+                ready_tokens=np.cumsum(np.bincount(first[has], minlength=E)), token_order=token_order)
+
+
+@pytest.mark.parametrize("T,k,E,G", [
+    (20, 4, 16, 2),        # one block, plain launch
+    (3000, 4, 32, 4),      # the grid, one staged chunk per block
+    (80000, 8, 64, 8),     # the grid, several staged chunks per block
+])
+def test_layout_skips_and_reports_invalid_ids_at_every_grid_shape(T, k, E, G):
+    rng = np.random.default_rng(T)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    bad = rng.random(ids.shape) < 0.01
+    ids[bad] = np.where(rng.random(int(bad.sum())) < 0.5, -1, E + rng.integers(0, 4, int(bad.sum())))
+    ids[0, 0] = E                                  # at least one of each kind
+    ids[-1, -1] = -1
+    w = rng.random((T, k)).astype(np.float32)
+    L, status = gu.gpu_layout(ids, w, E, G)
+    assert status.item() == moe.MOE_ERR_EXPERT_ID
+    want = layout_of_valid_pairs(ids, w, E, G)
+    got = L.numpy()
+    n = len(want["row_pair"])
+    assert np.array_equal(got["pair_row"], want["pair_row"])
+    assert np.array_equal(got["row_pair"][:n], want["row_pair"])
+    assert np.array_equal(got["row_weight"][:n].view(np.uint32), want["row_weight"].view(np.uint32))
+    assert np.array_equal(got["count"], want["count"])
+    assert np.array_equal(got["expert_offset"], want["expert_offset"])
+    assert np.array_equal(got["ready_tokens"], want["ready_tokens"])
+    assert np.array_equal(got["token_order"][: len(want["token_order"])], want["token_order"])
+
+
 @pytest.mark.parametrize("T,E,k,zipf", [(128, 8, 2, None), (2048, 256, 8, None), (4096, 256, 8, 1.2),
                                         (300, 1024, 16, None), (64, 40, 32, None)])
 def test_router_matches_oracle(T, E, k, zipf):
