@@ -57,13 +57,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       drain_fills(S, it, g.timeout_ns);
     } else if (warp == 1) {
-      mma_loop<true, !kGather>(S, KB, g.status, g.timeout_ns);
+      mma_loop<true, true>(S, KB, g.status, g.timeout_ns);
     } else if (kGather) {
       gather_a_loop(S, A, g.gather_row, g.H, KB, g.status, g.timeout_ns);
     }
   } else {
     regs_alloc<kRegsEpilogue>();
-    epilogue_loop<true, false, kGather, false, false, !kGather>(S, g);
+    epilogue_loop<true, false, kGather, false, false, true>(S, g);
   }
   gemm_teardown(S);
 }

@@ -279,13 +279,16 @@ MOE_DEV void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, in
 }
 
 // TMA warp, gathered A: W tile plus tile rows [0, kGatherTmaRows) (slots past
-// the unit's rows repeat its first row; their products are never stored).
+// the unit's rows repeat its first row; their products are never stored); a
+// unit of at most kSwapRows rows (run transposed) gathers rows [0, kSwapRows)
+// only.
 MOE_DEV bool produce_unit_gather(const GemmSmem& S, const CUtensorMap* tmA, const CUtensorMap* tmW,
                                  const int32_t* __restrict__ gather, const Unit& u, int KB, uint32_t& it,
                                  int32_t* status, uint64_t tmo) {
   GemmShared* sh = S.sh;
   const int lane = threadIdx.x & 31;
   const int first = gather[u.row0];
+  const int grows = u.rows <= kSwapRows ? kSwapRows : kGatherTmaRows;   // rows gathered by TMA
   int r4[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -299,11 +302,11 @@ MOE_DEV bool produce_unit_gather(const GemmSmem& S, const CUtensorMap* tmA, cons
     const uint32_t full = smem_u32(&sh->full[s]);
     const uint32_t dstA = smem_u32(S.stages + (size_t)s * kStageBytes);
     if (elect_one()) {
-      mbar_arrive_expect_tx(full, kBTileBytes + kGatherTmaRows * kGemmBK);
+      mbar_arrive_expect_tx(full, kBTileBytes + (uint32_t)grows * kGemmBK);
       tma_load_3d(dstA + kATileBytes, tmW, kb * kGemmBK, u.nb * kGemmBN, u.e, full);
     }
     __syncwarp();
-    if (lane < kGatherTmaRows / 4)
+    if (lane < grows / 4)
       tma_gather4(dstA + 512u * (uint32_t)lane, tmA, kb * kGemmBK, r4[0], r4[1], r4[2], r4[3], full);
     __syncwarp();
     ++it;
@@ -313,7 +316,8 @@ MOE_DEV bool produce_unit_gather(const GemmSmem& S, const CUtensorMap* tmA, cons
 
 // Gather warps (2 and 3): lane l copies tile rows kGatherTmaRows + l + 32 m of
 // the K-blocks of its parity.  Reads every unit from the ring like the MMA and
-// epilogue warps.
+// epilogue warps.  A unit run transposed reads only rows [0, kSwapRows), all
+// gathered by the TMA warp: the gather warp copies nothing and only arrives.
 MOE_DEV void gather_a_loop(const GemmSmem& S, const uint8_t* __restrict__ A, const int32_t* __restrict__ gather,
                            int H, int KB, int32_t* status, uint64_t tmo) {
   constexpr int kM = kGatherCopyRows / 32;
@@ -338,11 +342,17 @@ MOE_DEV void gather_a_loop(const GemmSmem& S, const uint8_t* __restrict__ A, con
       src[m] = A + (size_t)(r < rows ? gather[un.w + r] : 0) * H;
       nbytes[m] = r < rows ? 16u : 0u;
     }
+    const bool copy = rows > kSwapRows;
     for (int kb = 0; kb < KB; ++kb, ++it) {
       if ((it & 1u) != par) continue;
       const int s = (int)(it % kGemmStages);
       const uint32_t ph = (it / kGemmStages) & 1u;
       if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, &sh->abort_flag, status, tmo)) { ok = false; break; }
+      if (!copy) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh->full[s]));
+        continue;
+      }
       const uint32_t dst = smem_u32(S.stages + (size_t)s * kStageBytes);
 #pragma unroll
       for (int m = 0; m < kM; ++m) {
@@ -488,7 +498,7 @@ struct FoldAcc<true> {
 template <bool kPacked, bool kSignal = false, bool kGather = false, bool kPair = false, bool kReleaseStage = false,
           bool kSwap = false>
 MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
-  static_assert(!kSwap || (!kGather && !kPair), "transposed units: dense A, one CTA");
+  static_assert(!kSwap || !kPair, "transposed units: one CTA");
   GemmShared* sh = S.sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                 // TMEM lane quarter this warp may access
@@ -519,7 +529,7 @@ MOE_DEV void epilogue_loop(const GemmSmem& S, const GemmParams& g) {
     // nothing (zero-filled copies) from a clamped, valid address.  With A
     // gathered, a dense row's scales sit at its row of A.
     const uint32_t sa_row =
-        kGather ? (uint32_t)(valid ? g.gather_row[row0 + r_in_tile] : 0)
+        kGather ? (uint32_t)(valid ? g.gather_row[row0 + r_scale] : 0)
                 : (uint32_t)min((long long)(row0 + r_scale), (long long)g.R - 1);
     const uint32_t sa_bytes = valid ? 4u : 0u;
     const uint32_t sb_off = (uint32_t)((e * nsb + nb * 2 + h) * KB);
