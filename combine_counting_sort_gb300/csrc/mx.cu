@@ -236,6 +236,12 @@ constexpr uint32_t idesc_mxf8_e4m3(int M, int N) {
   return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
 }
 constexpr uint32_t kMxIdesc = idesc_mxf8_e4m3(kGemmBM, kGemmBN);
+// Transposed units (tiles of at most kSwapRows rows): W's two 128-row halves
+// as M = 128 operands with W's scale atoms, the tile's rows as N = 32 with
+// A's atom (rows 0..31 of an atom sit in lanes 0..31, as the N = 32 operand's
+// scale factors are read); the accumulator of W half h in columns
+// [h * kSwapRows, +kSwapRows).
+constexpr uint32_t kMxIdescSwap = idesc_mxf8_e4m3(kGemmBM, kSwapRows);
 
 MOE_DEV void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
                        uint32_t sfb_tmem, uint32_t accumulate) {
@@ -362,6 +368,7 @@ MOE_DEV void mx_mma_loop(const MxSmem& S, int KB, int32_t* status, uint64_t tmo)
     if (!mbar_wait(smem_u32(&sh->ufull[slot]), (uint32_t)(j / kUnitRing) & 1u, &sh->abort_flag, status, tmo))
       break;
     const int m = sh->unit[slot].x;
+    const bool swap = sh->unit_rows[slot] <= kSwapRows;
     __syncwarp();
     if (elect_one()) mbar_arrive(smem_u32(&sh->uempty[slot]));
     if (m < 0) break;
@@ -380,11 +387,21 @@ MOE_DEV void mx_mma_loop(const MxSmem& S, int KB, int32_t* status, uint64_t tmo)
       const uint32_t b0 = a0 + kATileBytes;
       const uint32_t tsf = tmem + kMxTmemSf + (uint32_t)s * kMxSfCols;
       if (elect_one()) {
+        if (swap) {
 #pragma unroll
-        for (int k4 = 0; k4 < kGemmBK / 32; ++k4)
-          umma_mxf8(tmem, sw128_kmajor_desc(a0 + k4 * 32), sw128_kmajor_desc(b0 + k4 * 32),
-                    kMxIdesc | ((uint32_t)k4 << 4) | ((uint32_t)k4 << 29), tsf, tsf + 4,
-                    (kb > 0 || k4 > 0) ? 1u : 0u);
+          for (int k4 = 0; k4 < kGemmBK / 32; ++k4)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              umma_mxf8(tmem + h * kSwapRows, sw128_kmajor_desc(b0 + h * (kBTileBytes / 2) + k4 * 32),
+                        sw128_kmajor_desc(a0 + k4 * 32), kMxIdescSwap | ((uint32_t)k4 << 4) | ((uint32_t)k4 << 29),
+                        tsf + 4 + 4 * h, tsf, (kb > 0 || k4 > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int k4 = 0; k4 < kGemmBK / 32; ++k4)
+            umma_mxf8(tmem, sw128_kmajor_desc(a0 + k4 * 32), sw128_kmajor_desc(b0 + k4 * 32),
+                      kMxIdesc | ((uint32_t)k4 << 4) | ((uint32_t)k4 << 29), tsf, tsf + 4,
+                      (kb > 0 || k4 > 0) ? 1u : 0u);
+        }
         umma_commit(smem_u32(&sh->empty[s]));   // the stage is free once these MMAs are done
       }
       __syncwarp();
@@ -422,6 +439,20 @@ MOE_DEV void mx_epilogue_loop(const MxSmem& S, const MxParams& p) {
     if (un.x < 0) return;
     if (!mbar_wait(smem_u32(&sh->tfull[0]), (uint32_t)j & 1u, &sh->abort_flag, p.status, p.timeout_ns)) return;
     tc_fence_after();
+    if (rows <= kSwapRows) {
+      // transposed unit: this thread's W row of half h, one column per token;
+      // stored as one output column (a warp covers 32 consecutive columns)
+      float v[32];
+      tmem_drain32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kSwapRows), v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[0]));
+      uint16_t* yc = p.Y + (size_t)un.w * p.N + (size_t)un.y * kGemmBN + h * 128 + q * 32 + lane;
+#pragma unroll
+      for (int t = 0; t < kSwapRows; ++t)
+        if (t < rows) yc[(size_t)t * p.N] = __bfloat16_as_ushort(__float2bfloat16_rn(v[t]));
+      continue;
+    }
     float acc[128];
     tmem_drain128(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128), acc);
     tc_fence_before();

@@ -47,6 +47,20 @@ def routed(cfg: inputs.MoEConfig):
     return oracle.router_topk(logits, cfg.k)
 
 
+def routing_with_counts(counts, seed=0):
+    """k = 1 routing whose expert e receives exactly counts[e] tokens, in a
+    seeded random token order; weights 1."""
+    ids = np.repeat(np.arange(len(counts), dtype=np.int32), counts)
+    np.random.default_rng(seed).shuffle(ids)
+    return ids[:, None].copy(), np.ones((len(ids), 1), np.float32)
+
+
+# Expert sizes around every boundary of the GEMM1 tile kinds: 1..32 rows
+# (transposed), 33..64 and 65..127 (short A boxes), 128 and more, and the last
+# tile of a larger expert on either side of 32 rows (160, 161).
+FEW_ROW_COUNTS = [1, 2, 7, 8, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 159, 160, 161, 0, 5, 3, 300, 30]
+
+
 def gpu_layout(ids: np.ndarray, w: np.ndarray, E: int, G: int):
     T, k = ids.shape
     L = moe.Layout(T, k, E, G)

@@ -92,22 +92,14 @@ def test_gemm1_small_full(T, H, E, G, k, N, skew):
     assert torch.isnan(r["Y"][r["R"]:].float()).all()
 
 
-def routing_with_counts(counts, seed=0):
-    """k = 1 routing whose expert e receives exactly counts[e] tokens, in a
-    seeded random token order; weights 1."""
-    ids = np.repeat(np.arange(len(counts), dtype=np.int32), counts)
-    np.random.default_rng(seed).shuffle(ids)
-    return ids[:, None].copy(), np.ones((len(ids), 1), np.float32)
-
-
 @pytest.mark.parametrize("H,N", [(512, 512), (256, 768)])
 def test_gemm1_few_row_tiles_full(H, N):
     """Tiles of 1..32 valid rows run transposed (W as the M = 128 operand, the
     tile's rows as N = 32), tiles of 33 and more as usual: expert sizes around
     every boundary (1, 31, 32, 33 rows; 128 + 32, 128 + 33 rows, whose last
     tile is short), every row checked against the oracle."""
-    counts = [1, 2, 7, 8, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 159, 160, 161, 0, 5, 3, 300, 30]
-    ids, w = routing_with_counts(counts, seed=5)
+    counts = gu.FEW_ROW_COUNTS
+    ids, w = gu.routing_with_counts(counts, seed=5)
     cfg = inputs.MoEConfig("few_rows", T=len(ids), H=H, E=len(counts), G=4, k=1, N=N, zipf=None, seed=5)
     W = inputs.make_weights(cfg.E, N, H, seed=5).cuda()
     r = run_stage1_unfused(cfg, W, ids, w)

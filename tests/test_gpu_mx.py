@@ -146,6 +146,21 @@ def test_mx_small_full(T, H, E, G, k, N, skew):
     assert torch.isnan(r["Y"][r["R"]:].float()).all()
 
 
+def test_mx_few_row_tiles_full():
+    """Tiles of 1..32 valid rows run transposed (W's halves as the M = 128
+    operands with W's scale atoms, the tile's rows as N = 32 with A's), the
+    others as usual: expert sizes around every boundary, every row checked."""
+    ids, w = gu.routing_with_counts(gu.FEW_ROW_COUNTS, seed=5)
+    cfg = inputs.MoEConfig("few_rows", T=len(ids), H=512, E=len(gu.FEW_ROW_COUNTS), G=4, k=1, N=512, zipf=None,
+                           seed=5)
+    W = inputs.make_weights(cfg.E, cfg.N, cfg.H, seed=5).cuda()
+    r = run_mx(cfg, W, ids=ids, w=w)
+    ref = check_dispatch(r, cfg)
+    want, _ = expected_gemm(cfg, r["x"], W, ref, np.arange(r["R"]))
+    gu.assert_close_bf16(gu.bits(r["Y"])[: r["R"]], want, "gemm1_mx")
+    assert torch.isnan(r["Y"][r["R"]:].float()).all()
+
+
 def sample_rows(eo, n_experts=6, seed=0):
     cnt = np.diff(eo)
     nz = np.nonzero(cnt)[0]
