@@ -16,11 +16,6 @@ namespace moe {
 // rows; half the tile rows gathered by the TMA warp, half copied by warps 2
 // and 3) instead of as 128-row boxes of the dense buffer; `A` is then the
 // send buffer.
-// A maps with boxes 32 and 64 rows high, for tiles with that few rows (dense A).
-struct ShortMaps {
-  CUtensorMap m[2];
-};
-
 template <bool kGather>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm1_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,

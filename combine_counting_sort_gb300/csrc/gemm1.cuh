@@ -185,6 +185,11 @@ MOE_DEV void gemm_teardown(const GemmSmem& S) {
   }
 }
 
+// A maps with boxes 32 and 64 rows high, for tiles with that few rows (dense A).
+struct ShortMaps {
+  CUtensorMap m[2];
+};
+
 // A unit handed from the producer thread to the MMA thread and the epilogue warps.
 struct Unit {
   int m, nb, e, row0, rows;

@@ -332,9 +332,18 @@ MOE_DEV void mx_sf_loop(const MxSmem& S, int KB, int units_here, int32_t* status
   }
 }
 
+// A tile of at most 32 (64) valid rows loads only that many A rows (the
+// 32- and 64-row maps of `tmA_short`): rows past the tile's end feed output
+// rows that are never stored.
 MOE_DEV bool mx_produce_unit(const MxSmem& S, const CUtensorMap* tmA, const CUtensorMap* tmW, const MxParams& p,
-                             const Unit& u, int KB, uint32_t& it) {
+                             const Unit& u, int KB, uint32_t& it, const CUtensorMap* tmA_short) {
   GemmShared* sh = S.sh;
+  const CUtensorMap* mapA = tmA;
+  uint32_t a_bytes = kATileBytes;
+  if (u.rows <= 64) {
+    mapA = u.rows <= 32 ? tmA_short : tmA_short + 1;
+    a_bytes = (u.rows <= 32 ? 32u : 64u) * kGemmBK;
+  }
   const int NB = p.N / 128;
   const uint8_t* sfa = p.A_sf + (size_t)u.m * KB * kMxSfaBytes;
   const uint8_t* sfb = p.W_sf + ((size_t)u.e * KB * NB + (size_t)u.nb * 2) * 512;
@@ -344,9 +353,9 @@ MOE_DEV bool mx_produce_unit(const MxSmem& S, const CUtensorMap* tmA, const CUte
     if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, &sh->abort_flag, p.status, p.timeout_ns)) return false;
     if (elect_one()) {
       const uint32_t full = smem_u32(&sh->full[s]);
-      mbar_arrive_expect_tx(full, kStageBytes + kMxSfStageBytes);
+      mbar_arrive_expect_tx(full, a_bytes + kBTileBytes + kMxSfStageBytes);
       const uint32_t dstA = smem_u32(S.stages + (size_t)s * kStageBytes);
-      tma_load_2d(dstA, tmA, kb * kGemmBK, u.row0, full);
+      tma_load_2d(dstA, mapA, kb * kGemmBK, u.row0, full);
       tma_load_3d(dstA + kATileBytes, tmW, kb * kGemmBK, u.nb * kGemmBN, u.e, full);
       const uint32_t dsf = smem_u32(S.sf + (size_t)s * kMxSfStageBytes);
       bulk_load(dsf, sfa + (size_t)kb * kMxSfaBytes, kMxSfaBytes, full);
@@ -470,7 +479,7 @@ MOE_DEV void mx_epilogue_loop(const MxSmem& S, const MxParams& p) {
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm1_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                            const __grid_constant__ MxParams p) {
+                            const __grid_constant__ ShortMaps tmS, const __grid_constant__ MxParams p) {
   extern __shared__ uint8_t smem_raw[];
   const MxSmem S = mx_smem(smem_raw);
   const int warp = threadIdx.x >> 5;
@@ -499,7 +508,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
         const Unit x = unit_of(p.L, u, nbn);
-        ok = publish_unit(S.sh, j, x, p.status, p.timeout_ns) && mx_produce_unit(S, &tmA, &tmW, p, x, KB, it);
+        ok = publish_unit(S.sh, j, x, p.status, p.timeout_ns) && mx_produce_unit(S, &tmA, &tmW, p, x, KB, it, tmS.m);
       }
       if (ok) {
         Unit end = {-1, 0, 0, 0, 0};
@@ -601,6 +610,13 @@ extern "C" int moe_grouped_gemm1_mx(const uint8_t* A, const uint8_t* A_sf, const
     if (!encode_u8_map(&tmA, A, 2, dA, sA, bA)) return MOE_ERR_CUDA;
     if (!encode_u8_map(&tmW, W, 3, dW, sW, bW)) return MOE_ERR_CUDA;
   }
+  ShortMaps tmS;
+  for (int i = 0; i < 2; ++i) {
+    const uint64_t dA[2] = {(uint64_t)H, (uint64_t)R};
+    const uint64_t sA[1] = {(uint64_t)H};
+    const uint32_t bA[2] = {kGemmBK, i == 0 ? 32u : 64u};
+    if (!encode_u8_map(&tmS.m[i], A, 2, dA, sA, bA)) return MOE_ERR_CUDA;
+  }
   MxParams p;
   p.A_sf = A_sf;
   p.W_sf = W_sf;
@@ -619,6 +635,6 @@ extern "C" int moe_grouped_gemm1_mx(const uint8_t* A, const uint8_t* A_sf, const
   if (cudaFuncSetAttribute(grouped_gemm1_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kMxSmemBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
-  grouped_gemm1_mx_kernel<<<grid, kGemmThreads, kMxSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, p);
+  grouped_gemm1_mx_kernel<<<grid, kGemmThreads, kMxSmemBytes, (cudaStream_t)stream>>>(tmA, tmW, tmS, p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
