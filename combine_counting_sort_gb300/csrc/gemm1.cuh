@@ -19,15 +19,21 @@
 //                    one of two TMEM partial buffers (2 x 256 columns), one
 //                    commit to the smem stage's empty barrier (the stage goes
 //                    back to the TMA thread as soon as the MMAs that read it
-//                    are done) and one to that buffer's partial-ready barrier.
+//                    are done) and one to that buffer's partial-ready barrier;
+//                    a tile of at most kSwapRows rows runs transposed instead
+//                    (8 MMAs of M=128, N=32 per K-block: W's two halves times
+//                    the tile's rows, see kSwapRows).
 //   warps 2, 3       idle (they complete warpgroup 0, whose registers go to
-//                    the promotion warpgroups: setmaxnreg 40 / 232).
+//                    the promotion warpgroups: setmaxnreg 40 / 232), or, with
+//                    A gathered row by row, copying half of each A tile.
 //   warps 4..11      promotion: each thread owns one row (TMEM lane) and 128
 //                    columns; per K-block it loads the fp32 partial and folds it
 //                    into register accumulators with the two block scales,
 //                    acc += partial * (sa[row, kb] * sb[e, n/128, kb]), the two
 //                    scales fetched ahead by cp.async; after the last K-block it
-//                    rounds to bf16 and stores the valid rows.
+//                    rounds to bf16 and stores the valid rows (a transposed
+//                    tile: one W row's 32 token columns per thread, each with
+//                    its token's scale, stored as one output column).
 //
 // fp32 block scales per 128 values are not a tensor-core mode (the hardware
 // block-scaled kinds take power-of-two scales per 32), so the scales are
